@@ -1,0 +1,84 @@
+"""The five workloads of the MoE-layer hot path, by name and size.
+
+tiny          H=256,  I=128,  E=16,  top-4, 4 groups / 2 kept, 1 token, fp32 x
+glm_decode    H=6144, I=2048, E=256, top-8, 8 groups / 4 kept, T=1, 256 tokens
+glm_verify    same layer, T=4 correlated tokens per step (1 accepted + 3 drafts)
+glm_prefill   same layer, T=512 tokens in one call
+glm_stack     24 such layers resident, T=1, RMSNorm before each router and a
+              residual add after each layer
+
+GLM-5.2 layer geometry (256 routed experts, top-8, one shared expert,
+routed_scaling_factor, sigmoid noaux_tc routing): "GLM-5.2 on a 32 GB Mac"
+section "What Colibri is actually doing" and "N1. GLM-5.2 graph"; the Colibri
+README "What's implemented".  Hidden/intermediate sizes, group limits and the
+int4 group-32 fp16-scale format are the workload's own fixed sizes.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    hidden: int
+    inter: int
+    n_experts: int
+    top_k: int
+    n_group: int
+    topk_group: int
+    routed_scaling_factor: float
+    n_shared: int = 1
+    shared_inter: int = 0  # 0 -> same as inter
+    group_size: int = 32
+
+    @property
+    def i_shared(self) -> int:
+        return self.shared_inter or self.inter
+
+    def expert_bytes(self) -> int:
+        """Packed nibbles + fp16 group scales of one routed expert."""
+        h, i, g = self.hidden, self.inter, self.group_size
+        packed = 3 * h * i // 2
+        scales = 2 * (i * h // g) * 2 + (h * i // g) * 2
+        return packed + scales
+
+    def shared_bytes(self) -> int:
+        h, i, g = self.hidden, self.i_shared, self.group_size
+        return 3 * h * i // 2 + 3 * (h * i // g) * 2
+
+    def router_bytes(self) -> int:
+        return self.n_experts * self.hidden * 4 + self.n_experts * 4
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    shape: LayerShape
+    tokens_per_call: int  # T of one forward call
+    calls: int  # forward calls in one pass of the workload
+    x_dtype: str  # "f32" or "bf16"
+    bias_kind: str  # "uniform" or "zipf"
+    seed: int
+    layers: int = 1
+    correlated: float = 0.0  # per-token noise amplitude for verify batches
+    rmsnorm_eps: float = 0.0  # >0: RMSNorm before the router + residual add
+    zipf_s: float = 1.1
+    extra: dict = field(default_factory=dict)
+
+
+TINY = LayerShape(256, 128, 16, 4, 4, 2, 2.5)
+GLM = LayerShape(6144, 2048, 256, 8, 8, 4, 2.5)
+
+CONFIGS = {
+    "tiny": Workload("tiny", TINY, 1, 1, "f32", "uniform", 1001),
+    "glm_decode": Workload("glm_decode", GLM, 1, 256, "bf16", "zipf", 1002),
+    "glm_verify": Workload("glm_verify", GLM, 4, 64, "bf16", "zipf", 1003,
+                           correlated=0.3),
+    "glm_prefill": Workload("glm_prefill", GLM, 512, 1, "bf16", "zipf", 1004),
+    "glm_stack": Workload("glm_stack", GLM, 1, 16, "f32", "zipf", 5000,
+                          layers=24, rmsnorm_eps=1e-5),
+}
+
+
+def config_by_name(name: str) -> Workload:
+    return CONFIGS[name]
