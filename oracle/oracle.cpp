@@ -42,8 +42,9 @@
 //   R8  group size 32 along K, fp16 scales.
 //   R9  shared expert weight 1, added after the routed sum.
 //   R12 plan order: experts ascending, entries (t, j) ascending.
-//   R13 RMSNorm: fixed fp64 sum order stated at rmsnorm_row(); gamma is
-//       multiplicative; normalised activations stay fp32.
+//   R13 RMSNorm: fixed fp64 sum order stated at rmsnorm_row(); the
+//       reciprocal root is rounded to fp32 and applied with fp32 products;
+//       gamma is multiplicative; normalised activations stay fp32.
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC.
 // Contraction must stay off: every fused multiply-add below is written as
@@ -290,9 +291,10 @@ int oracle_plan(const int32_t* ids, int T, int k, int E, int32_t* counts,
 // multiplicative weight, double-accumulated reduction).  The fp64 sum of
 // squares uses the same fixed order as router_logit (8 segments x 32
 // partials over chunks of 4, fused multiply-adds, pairwise halving); then
-//   r = 1 / sqrt(ss / H + eps)         (fp64, each step rounded)
-//   out_k = (float)(h_k * r) * gamma_k (fp64 product rounded to fp32, then an
-//                                       fp32 product with gamma)
+//   r  = 1 / sqrt(ss / H + eps)        (fp64, each step rounded)
+//   rf = (float)r                      (the pages keep only the reduction in
+//                                       double; the scaling is fp32)
+//   out_k = (h_k * rf) * gamma_k       (two fp32 products, each rounded)
 void rmsnorm_row(const float* h, int H, const float* gamma, double eps, float* out) {
   const int L = H / 8;
   const int chunks = L / 4;
@@ -316,8 +318,9 @@ void rmsnorm_row(const float* h, int H, const float* gamma, double eps, float* o
     for (int s = 0; s < d; ++s) seg[s] = seg[s] + seg[s + d];
   const double mean = seg[0] / (double)H;
   const double r = 1.0 / std::sqrt(mean + eps);
+  const float rf = (float)r;
   for (int k = 0; k < H; ++k) {
-    const float v = (float)((double)h[k] * r);
+    const float v = h[k] * rf;
     out[k] = gamma ? v * gamma[k] : v;
   }
 }
