@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Throughput of the int4 routed-expert MoE layer on GB300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl gb300|reference]
+
+One step = one pass of the workload: for the default glm_decode workload, 256
+independent tokens, each one moe_forward call (T = 1) of the GLM-5.2-shaped
+layer (router, plan, 8 routed experts + shared expert, combine).  Inputs are
+seeded synthetic tensors resident in HBM.  L2 is flushed (512 MiB read)
+before every forward, outside the timed events, so that no expert weight is
+served from L2.  `value` = tokens of all ranks / max-over-ranks device time.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(weak scaling, no data-path collective: the layer does not shard).
+`--impl reference` times the CPU oracle (the reference arm) on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s (% of ~8 TB/s peak) on 1 GB300"
+UNIT = "tokens/s"
+FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ------------------------------------------------------------------ helpers --
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm = []
+        mx = None
+        reasons = set()
+        names = ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+        for p in self.samples:
+            try:
+                sm.append(float(p[0]))
+                mx = float(p[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_routed_expert_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != kernel_source_hash():
+        return None
+    return t.get("per_launch_bytes", {}).get(f"{workload}:{kernel}")
+
+
+# ----------------------------------------------------- algorithmic bytes ----
+
+def expert_gate_up_bytes(sh):
+    return 2 * (sh.inter * sh.hidden // 2 + sh.inter * sh.hidden // 32 * 2)
+
+
+def expert_down_bytes(sh, inter=None):
+    I = inter or sh.inter
+    return sh.hidden * I // 2 + sh.hidden * I // 32 * 2
+
+
+def phase_bytes(phase, sh, T, n_act, x_bytes):
+    """Algorithmic HBM bytes of one launch of a phase (weights read once,
+    activations read once, outputs written once)."""
+    H, E, k = sh.hidden, sh.n_experts, sh.top_k
+    ns = 1 if sh.n_shared else 0
+    router = E * H * 4 + E * 4
+    hrows = (T * k + T * ns) * sh.inter * 4
+    if phase == "decode_router_gate_up":
+        return router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh) + hrows
+    if phase == "decode_down_combine":
+        return (n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
+                + hrows + T * H * 4)
+    if phase == "gate_up":
+        return (n_act + ns) * expert_gate_up_bytes(sh) + T * H * 4 + hrows
+    if phase == "down":
+        return (n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
+                + hrows + (T * k + T * ns) * H * 4)
+    return None
+
+
+# ------------------------------------------------------------- workloads ----
+
+def make_workload(name, experts=None, calls=None):
+    from workloads import CONFIGS
+    from workloads.configs import LayerShape, Workload
+    wl = CONFIGS[name]
+    if experts or calls:
+        sh = wl.shape
+        if experts:
+            sh = LayerShape(sh.hidden, sh.inter, experts, sh.top_k, sh.n_group, sh.topk_group,
+                            sh.routed_scaling_factor, sh.n_shared, sh.shared_inter,
+                            sh.group_size)
+        wl = Workload(wl.name, sh, wl.tokens_per_call, calls or wl.calls, wl.x_dtype,
+                      wl.bias_kind, wl.seed, wl.layers, wl.correlated, wl.rmsnorm_eps,
+                      wl.zipf_s)
+    return wl
+
+
+class GpuRun:
+    """Resident layers, inputs and outputs of one workload on one device."""
+
+    def __init__(self, wl, dev, layers=None):
+        import torch
+
+        import int4_routed_expert_gb300 as m
+        from workloads.gen import gen_activations, gen_layer, gen_norm_weight
+        self.m, self.wl, self.dev = m, wl, dev
+        sh = wl.shape
+        self.T = wl.tokens_per_call
+        self.calls = wl.calls
+        self.n_layers = layers or wl.layers
+        self.layers = [gen_layer(wl, layer=i, device=dev) for i in range(self.n_layers)]
+        self.handles = [m.MoELayer(L, self.T) for L in self.layers]
+        self.norm = wl.rmsnorm_eps > 0
+        self.gammas = ([gen_norm_weight(wl, i).to(dev) for i in range(self.n_layers)]
+                       if self.norm else [None] * self.n_layers)
+        xs = [gen_activations(wl, self.T, call=c, dtype="f32" if self.norm else None)
+              for c in range(self.calls)]
+        self.x_host = torch.stack(xs).pin_memory()           # [calls, T, H]
+        self.x = self.x_host.to(dev)
+        self.x_bytes = self.x.element_size()
+        self.y = torch.empty(self.calls, self.T, sh.hidden, dtype=torch.float32, device=dev)
+        self.y_host = torch.empty_like(self.y, device="cpu").pin_memory()
+        self.flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_buf.fill_(1.0)
+        self.flush_out = torch.empty((), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def flush(self):
+        import torch
+        torch.sum(self.flush_buf, dim=0, out=self.flush_out)
+
+    def forward(self, c):
+        """Layer stack on call c: y = MoE(x) (or the residual stack in place)."""
+        if not self.norm:
+            for h in self.handles:
+                h.forward(self.x[c], y=self.y[c], stream=self.stream)
+        else:
+            y = self.y[c]
+            y.copy_(self.x[c])
+            for h, g in zip(self.handles, self.gammas):
+                h.forward(y, y=y, gamma=g, eps=self.wl.rmsnorm_eps, accumulate=True,
+                          stream=self.stream)
+
+    def timed_pass(self, e2e=False):
+        """Device ms of one step: sum over calls of the forward's events."""
+        import torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(self.calls)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(self.calls)]
+        for c in range(self.calls):
+            self.flush()
+            starts[c].record()
+            if e2e:
+                self.x[c].copy_(self.x_host[c], non_blocking=True)
+            self.forward(c)
+            if e2e:
+                self.y_host[c].copy_(self.y[c], non_blocking=True)
+            ends[c].record()
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+    def traced_pass(self):
+        """Per-phase device ms (summed over the step) and launches per step."""
+        import torch
+        m = self.m
+        for h in self.handles:
+            m.moe_trace_enable(h.h, self.calls)
+        for c in range(self.calls):
+            self.flush()
+            self.forward(c)
+        torch.cuda.synchronize()
+        phase_ms, launches, n_phase = {}, 0, {}
+        for h in self.handles:
+            names, rows = m.moe_trace_read(h.h, self.calls)
+            for row in rows:
+                for n, v in zip(names, row):
+                    if v > 0:
+                        phase_ms[n] = phase_ms.get(n, 0.0) + v
+                        n_phase[n] = n_phase.get(n, 0) + 1
+                        launches += 1
+            m.moe_trace_enable(h.h, 0)
+        return phase_ms, n_phase, launches
+
+    def active_experts(self):
+        """Mean distinct experts per call (from the plan of each call)."""
+        import torch
+        m = self.m
+        sh = self.wl.shape
+        tot = 0
+        for c in range(min(self.calls, 32)):
+            plan = m.Plan(self.T, sh.top_k, sh.n_experts, self.dev)
+            x = self.x[c] if not self.norm else self.y[c]
+            self.handles[0].route(x, gamma=self.gammas[0], eps=self.wl.rmsnorm_eps or 1e-5,
+                                  plan=plan)
+            tot += int(plan.n_active.item())
+        torch.cuda.synchronize()
+        return tot / min(self.calls, 32)
+
+    def check_status(self):
+        for h in self.handles:
+            self.m.moe_device_status(h.h)
+
+
+# ------------------------------------------------------------ oracle arm ----
+
+class OracleArm:
+    """The CPU oracle (single-thread C++) on sample tokens of the workload.
+
+    Expert regeneration is input preparation, not the oracle's work: the
+    experts the sample selects are generated before anything is timed."""
+
+    def __init__(self, wl, n_calls):
+        import numpy as np
+
+        import oracle
+        from workloads.gen import (SHARED_EXPERT, HostExpertCache, gen_activations,
+                                   gen_norm_weight, gen_router)
+        self.oracle, self.shared_id, self.wl = oracle, SHARED_EXPERT, wl
+        sh = wl.shape
+        self.norm = wl.rmsnorm_eps > 0
+        # a bounded sample: at most 4 token rows of a call, at most 2 stacked layers
+        self.rows = min(wl.tokens_per_call, 4)
+        self.layers_run = 1 if not self.norm else min(wl.layers, 2)
+        self.eps = float(np.float32(wl.rmsnorm_eps)) if self.norm else 0.0
+        self.caches = [HostExpertCache(wl, i) for i in range(self.layers_run)]
+        self.routers, self.gammas = [], []
+        for i in range(self.layers_run):
+            seed = wl.seed + i if wl.layers > 1 else wl.seed
+            rw, rb = gen_router(sh, seed, i, wl.bias_kind, wl.zipf_s)
+            self.routers.append((rw.numpy(), rb.numpy()))
+            self.gammas.append(gen_norm_weight(wl, i).numpy() if self.norm else None)
+        self.xs = [np.ascontiguousarray(
+            gen_activations(wl, wl.tokens_per_call, call=c,
+                            dtype="f32" if self.norm else None).float().numpy()[:self.rows])
+            for c in range(n_calls)]
+        for c in range(n_calls):
+            h = self.xs[c]
+            for i in range(self.layers_run):
+                self._forward(i, h, warm=True)
+                h = self._forward(i, h)
+
+    def _forward(self, i, h, warm=False):
+        if warm:
+            _, _, ids, _ = self.oracle.route(self.wl.shape, *self.routers[i], h, self.eps,
+                                             self.gammas[i])
+            for e in set(ids.reshape(-1).tolist()) | {self.shared_id}:
+                self.caches[i].expert(e)
+            return None
+        y, _, _, _ = self.oracle.moe_forward(
+            self.wl.shape, *self.routers[i], self.caches[i].expert,
+            self.caches[i].expert(self.shared_id), h, eps=self.eps, gamma=self.gammas[i],
+            resid=h if self.norm else None)
+        return y
+
+    def run(self, c):
+        """Seconds per token through the whole layer stack, for call c."""
+        t0 = time.perf_counter()
+        h = self.xs[c % len(self.xs)]
+        for i in range(self.layers_run):
+            h = self._forward(i, h)
+        dt = time.perf_counter() - t0
+        return dt / self.rows * (self.wl.layers / self.layers_run)
+
+    def describe(self):
+        return (f"{self.rows} token row(s) per call of {self.wl.name}, {self.layers_run} of "
+                f"{self.wl.layers} layer(s) timed and scaled to the stack, single-thread C++ "
+                "oracle, fp32 accumulation")
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    arm = OracleArm(wl, min(args.steps + args.warmup, 8))
+    for w in range(args.warmup):
+        arm.run(w)
+    s_per_tok = 0.0
+    for k in range(args.steps):
+        s_per_tok += arm.run(args.warmup + k)
+    value = args.steps / s_per_tok
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * s_per_tok / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "sample": arm.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": arm.describe()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- main arm ----
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="glm_decode",
+                    choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack"])
+    ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
+    ap.add_argument("--calls", type=int, default=None, help="override calls per step")
+    ap.add_argument("--layers", type=int, default=None, help="override stacked layers")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = make_workload(args.workload, args.experts, args.calls)
+
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    run = GpuRun(wl, dev, args.layers)
+    sh = wl.shape
+    for _ in range(max(args.warmup, 3)):
+        run.timed_pass()
+    run.check_status()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    dev_ms = 0.0
+    for _ in range(args.steps):
+        dev_ms += run.timed_pass()
+    barrier()
+    clocks.stop()
+    run.check_status()
+
+    # end to end: inputs copied from pinned host memory and outputs read back
+    # inside each forward's events
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        e2e_ms += run.timed_pass(e2e=True)
+    run.check_status()
+
+    if world > 1:
+        t = torch.tensor([dev_ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev_ms, e2e_ms = float(t[0]), float(t[1])
+
+    tokens_step = wl.tokens_per_call * wl.calls
+    value = world * tokens_step * args.steps / (dev_ms / 1000.0)
+    e2e_value = world * tokens_step * args.steps / (e2e_ms / 1000.0)
+
+    phase_ms, n_phase, launches_step = run.traced_pass()
+    n_act = run.active_experts()
+    peak, peak_kind = measured_peaks()
+    dominant = max(phase_ms, key=phase_ms.get)
+    per_launch_ms = phase_ms[dominant] / n_phase[dominant]
+    T = wl.tokens_per_call
+    kb = phase_bytes(dominant, sh, T, n_act, run.x_bytes)
+    kernels = {}
+    for name, ms in phase_ms.items():
+        b = phase_bytes(name, sh, T, n_act, run.x_bytes)
+        avg = ms / n_phase[name]
+        kernels[name] = {"avg_us": round(1000 * avg, 3), "launches_per_step": n_phase[name],
+                         "share": round(ms / sum(phase_ms.values()), 4)}
+        if b:
+            kernels[name]["algorithmic_bytes"] = b
+            kernels[name]["achieved_gbs"] = round(b / (avg / 1000.0) / 1e9, 1)
+    layer_bytes = sum(phase_bytes(n, sh, T, n_act, run.x_bytes) or 0 for n in phase_ms)
+    ms_per_call = dev_ms / (args.steps * wl.calls * max(1, run.n_layers))
+    layer_gbs = layer_bytes / (ms_per_call / 1000.0) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_calls = 8 if T == 1 else 2
+        arm = OracleArm(wl, n_calls)
+        s_tok = sum(arm.run(c) for c in range(n_calls)) / n_calls
+        cpu = {"value": 1.0 / s_tok, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_calls} call(s): " + arm.describe()}
+
+    if rank == 0:
+        achieved = kb / (per_launch_ms / 1000.0) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": dev_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded int4 weights, fp16 scales, Zipf router bias)",
+            "config": {
+                "workload": wl.name, "hidden": sh.hidden, "inter": sh.inter,
+                "n_experts": sh.n_experts, "top_k": sh.top_k, "layers": run.n_layers,
+                "tokens_per_call": T, "calls_per_step": wl.calls,
+                "tokens_per_step": tokens_step, "x_dtype": "f32" if run.norm else wl.x_dtype,
+                "weights": "int4 offset-binary, group 32, fp16 scales",
+                "l2": "flushed (512 MiB read) before every forward, outside the events",
+                "parallelism": f"replicas x{world}",
+            },
+            "roofline": {"bound": "hbm", "kernel": dominant,
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "traffic": ncu_traffic(dominant, wl.name),
+                         "algorithmic_bytes_per_launch": kb,
+                         "avg_launch_us": round(1000 * per_launch_ms, 3),
+                         "duration_source": "CUDA events between the kernels in a traced pass "
+                                            "of the same step right after the timed region"},
+            "layer_hbm": {"bytes_per_call": layer_bytes, "gbs": round(layer_gbs, 1),
+                          "pct_of_8tbs": round(100 * layer_gbs / NOMINAL_HBM_GBS, 1),
+                          "frac_of_measured": round(layer_gbs / peak, 4),
+                          "mean_active_experts": n_act},
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": int(run.x[0].numel() * run.x_bytes * wl.calls),
+                    "d2h_bytes_per_step": int(run.y[0].numel() * 4 * wl.calls)},
+            "gpu_launches": launches_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

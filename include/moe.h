@@ -1,0 +1,206 @@
+/*
+ * moe.h - C ABI of the int4 routed-expert MoE layer for one NVIDIA GB300
+ * (sm_103a).  One layer forward: noaux_tc sigmoid router with score
+ * correction bias and group-limited top-k, renormalised gate weights times
+ * routed_scaling_factor, a bit-exact routing plan, int4 group-32
+ * dequant -> fp32 SwiGLU routed experts, the weighted combine and the
+ * always-on shared expert.
+ *
+ * What the operations are (page title, then section):
+ *  - "GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri hierarchy",
+ *    N1 "GLM-5.2 graph" (MoE bullet): sigmoid scores plus correction bias
+ *    select, the un-biased sigmoid weights, true top-8, optional
+ *    normalisation / routed scale, shared expert in parallel.
+ *  - same page, "G2 implementation status": offset-binary Q4
+ *    (bias = -8 * scale), lower expert id wins exact ties, unweighted shared
+ *    expert; "G2 - native GLM-5.2 correctness spine": dequant -> f32
+ *    multiply-accumulate.
+ *  - same page, N4 "Scheduling and prediction" and "G3 implementation
+ *    status": route the whole batch first, stable unique expert union, each
+ *    expert run once over every row that chose it, rows composed in route
+ *    order.
+ *  - "colibri-strix/README.md", "What's implemented": DeepSeek-V3-style
+ *    sigmoid router (noaux_tc, routed_scaling_factor), shared expert,
+ *    batch-union MoE; "Experimental resident CUDA backend": invalid requests
+ *    fail instead of silently falling back.
+ *  - "Model support - run anything mlx-lm runs", 6.4 "GLM-5.2": RMSNorm with
+ *    multiplicative weight and double-accumulated reduction.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers unless stated otherwise; the
+ *    caller owns them.  Weights are borrowed: they must stay valid and
+ *    unchanged until moe_destroy.  The library never copies or repacks them.
+ *  - Work is enqueued on the given stream (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and returns without synchronising.
+ *  - Argument, shape and capacity errors are detected on the host before
+ *    any launch and return a negative moe_status_t; nothing is launched then.
+ *    MOE_ERR_CUDA reports a CUDA error (message in moe_last_error).
+ *  - A handle is not re-entrant: do not call it from two host threads at
+ *    once, and do not have two of its calls in flight on different streams
+ *    (they share the handle's workspace).
+ *  - There is no CPU fallback: without a usable GB300 every call fails.
+ *
+ * Data formats:
+ *  - int4 weights: symmetric q in [-8, 7] stored offset-binary u = q + 8,
+ *    two per byte, the low nibble holding the even K index.  Rows are
+ *    K-contiguous.  One fp16 scale (IEEE binary16 bits) per 32 consecutive K
+ *    of a row; dequantised value = (u - 8) * scale.
+ *  - Routed expert tensors are stacked over experts: gate/up
+ *    [E][I][H/2] bytes + [E][I][H/32] scales, down [E][H][I/2] +
+ *    [E][H][I/32].  Shared expert: the same without the E dimension, with
+ *    I = shared_inter.
+ *  - Router weight fp32 [E][H] row-major, bias fp32 [E].
+ *  - Activations x: [T][H] fp32 or bf16, row-major.  Output y: [T][H] fp32.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* NULL pointer, negative size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2, /* shape outside what the kernels handle */
+  MOE_ERR_CAPACITY = -3,    /* T > max_tokens of the handle */
+  MOE_ERR_CUDA = -4,        /* a CUDA call failed; see moe_last_error */
+  MOE_ERR_OOM = -5          /* workspace allocation failed at create */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Layer geometry.  Requirements (else MOE_ERR_UNSUPPORTED):
+ *   hidden % 256 == 0 and 256 <= hidden <= 16384;
+ *   inter % 32 == 0, shared_inter % 32 == 0 (if n_shared), both <= 8192;
+ *   1 <= n_experts <= 1024, n_experts % n_group == 0;
+ *   1 <= topk_group <= n_group, 1 <= top_k <= 32,
+ *   top_k <= topk_group * (n_experts / n_group);
+ *   group_size == 32; n_shared in {0, 1}; 1 <= max_tokens <= 65536. */
+typedef struct {
+  int hidden;                  /* H */
+  int inter;                   /* I, routed expert intermediate size */
+  int n_experts;               /* E */
+  int top_k;                   /* k */
+  int n_group;                 /* expert groups for the group limit */
+  int topk_group;              /* groups kept per token */
+  float routed_scaling_factor; /* multiplies the renormalised gate weights */
+  int n_shared;                /* 0 or 1 always-on shared expert */
+  int shared_inter;            /* shared expert intermediate size */
+  int group_size;              /* quantisation group along K; must be 32 */
+  int max_tokens;              /* largest T any call on this handle may pass */
+} moe_config_t;
+
+/* Device pointers, borrowed for the handle's lifetime.  Every pointer must
+ * be 16-byte aligned.  sh_* may be NULL when n_shared == 0. */
+typedef struct {
+  const float* router_w;    /* [E][H] fp32 */
+  const float* router_bias; /* [E] fp32 score-correction bias */
+  const uint8_t* gate_q;    /* [E][I][H/2] */
+  const uint16_t* gate_s;   /* [E][I][H/32] fp16 bits */
+  const uint8_t* up_q;      /* [E][I][H/2] */
+  const uint16_t* up_s;     /* [E][I][H/32] */
+  const uint8_t* down_q;    /* [E][H][I/2] */
+  const uint16_t* down_s;   /* [E][H][I/32] */
+  const uint8_t* sh_gate_q; /* [Is][H/2] */
+  const uint16_t* sh_gate_s;
+  const uint8_t* sh_up_q;   /* [Is][H/2] */
+  const uint16_t* sh_up_s;
+  const uint8_t* sh_down_q; /* [H][Is/2] */
+  const uint16_t* sh_down_s;
+} moe_weights_t;
+
+/* Routing outputs (device, caller-owned; any member may be NULL to skip it).
+ *   topk_ids [T][k] int32  selected experts, biased score descending, ties
+ *                          to the lower id
+ *   topk_w   [T][k] fp32   gate weights (un-biased sigmoid, renormalised
+ *                          over the k, times routed_scaling_factor)
+ *   counts   [E]    int32  entries routed to each expert
+ *   offsets  [E+1]  int32  exclusive prefix sum of counts
+ *   perm     [T*k]  int32  entry indices i = t*k + j grouped by expert
+ *                          ascending, ascending i inside an expert
+ *   active   [E]    int32  experts with count > 0, ascending (first
+ *                          n_active entries are written)
+ *   n_active [1]    int32 */
+typedef struct {
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* active;
+  int32_t* n_active;
+} moe_plan_t;
+
+typedef struct moe_layer moe_layer_t;
+
+/* Validate cfg and w, allocate the handle's device workspace (sized for
+ * cfg->max_tokens) on the current CUDA device, and return the handle in
+ * *out.  On failure *out is set to NULL and the message is available from
+ * moe_last_error(NULL) on this thread. */
+moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
+                              moe_layer_t** out);
+
+/* Route T tokens (RMSNorm first when rms_gamma is given, see moe_forward):
+ * logits, selection and the routing plan.  x: [T][H] of dtype.  T == 0 is a
+ * no-op.  Outputs go to the non-NULL members of *plan_out. */
+moe_status_t moe_route(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
+                       const float* rms_gamma, float rms_eps, moe_plan_t* plan_out,
+                       void* stream);
+
+/* Full layer forward on T tokens:
+ *   x_hat = rms_gamma ? RMSNorm(x) * rms_gamma : x  (eps = rms_eps; the sum
+ *           of squares is reduced in fp64)
+ *   y     = (accumulate ? y : 0) + sum_j w_tj * E_{id_tj}(x_hat_t) + S(x_hat_t)
+ * where E_e is routed expert e's SwiGLU and S the shared expert.  y: [T][H]
+ * fp32.  y may alias x only for the residual-stream form (dtype MOE_F32,
+ * accumulate = 1, rms_gamma != NULL, y == x exactly); otherwise they must
+ * not overlap.  plan_out may be NULL.  T == 0 is a no-op. */
+moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
+                         float* y, const float* rms_gamma, float rms_eps, int accumulate,
+                         moe_plan_t* plan_out, void* stream);
+
+/* Free the workspace and the handle.  Waits for the handle's work to finish
+ * (device synchronise).  NULL is ignored. */
+void moe_destroy(moe_layer_t* h);
+
+/* Last error message of the handle (or of this thread when h == NULL). */
+const char* moe_last_error(const moe_layer_t* h);
+
+/* Bytes of device workspace moe_layer_create allocates for cfg (0 if cfg is
+ * invalid). */
+size_t moe_workspace_bytes(const moe_config_t* cfg);
+
+/* Phase tracing (CUDA events between the kernels of moe_forward).
+ * moe_trace_enable(h, n): when n > 0, the next n moe_forward calls each
+ * record one CUDA event before their first kernel and one after every
+ * kernel, on the call's stream; later calls are not traced.  A traced call
+ * launches its kernels without the programmatic-dependent-launch overlap so
+ * that each duration belongs to one kernel.  n == 0 disables and frees the
+ * events.  Returns MOE_ERR_INVALID_ARG for n < 0 or n > 65536.
+ * moe_trace_read(h, ms, cap, n_calls, n_phases): waits for the traced calls
+ * (cudaEventSynchronize), writes the duration in milliseconds of phase p of
+ * traced call c to ms[c * n_phases + p] for c < min(cap, traced calls)
+ * (0 for phases the call did not run), stores the counts, and restarts the
+ * trace for the next n calls.  ms must hold cap * n_phases floats, with
+ * n_phases = 10 (the phase ids of moe_trace_phase_name).
+ * moe_trace_phase_name(p): static name of phase p (NULL when out of range).
+ * Tracing is off by default. */
+moe_status_t moe_trace_enable(moe_layer_t* h, int n_calls);
+moe_status_t moe_trace_read(moe_layer_t* h, float* ms, int cap, int* n_calls, int* n_phases);
+const char* moe_trace_phase_name(int phase);
+
+/* Device-side status: copies the handle's device error word to *flags
+ * (synchronous), clears it, and returns MOE_ERR_CUDA when it was non-zero.
+ * Bit 0: a bounded wait inside a kernel gave up (about one second) and the
+ * kernel returned early; the outputs of that call are not valid. */
+moe_status_t moe_device_status(moe_layer_t* h, int32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

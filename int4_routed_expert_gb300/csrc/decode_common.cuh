@@ -1,0 +1,295 @@
+// Fused small-batch path (T <= 4 tokens, T*k <= 32 entries): shared
+// definitions of its two kernels.
+//
+//   dec_ab  (cooperative, one CTA per SM)  router logits of the CTA's
+//           experts -> grid barrier -> every warp re-derives the selection
+//           and the routing plan in registers -> gate/up rows of the shared
+//           expert (streamed while the router runs) and of the selected
+//           experts -> h = SiLU(g) * u, written pre-scaled and swizzled.
+//   dec_c   (programmatic dependent launch) down-projection rows of every
+//           selected expert and the shared expert, weighted by the gate
+//           weights, summed into y.
+//
+// "GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri hierarchy", N1
+// (MoE bullet), N2 (packed int4 gate/up/down with grouped scales), N4 (route
+// the batch first, stream the union of the selected experts once);
+// "colibri-strix/README.md", "What's implemented" (noaux_tc router, shared
+// expert, batch-union MoE).
+#pragma once
+
+#include "moe_internal.cuh"
+#include "router_math.cuh"
+#include "stream_common.cuh"
+
+namespace moe {
+namespace dec {
+
+constexpr int kMaxEntries = 32;       // T * k
+constexpr int kMaxNT = 4;             // tokens per call
+constexpr int kRowsC = 4;             // down-projection rows per item
+constexpr int kMaxLocalExperts = 8;   // router experts per CTA
+constexpr int kRouterWarps = 8;       // one warp per logit segment
+
+struct DecArgs {
+  moe_weights_t w;
+  Shape sh;
+  int T;
+  const void* x;
+  int dt;
+  const float* gamma;
+  float eps;
+  Workspace ws;
+  float* y;
+  int accumulate;
+  unsigned long long gtarget;  // grid-barrier count that completes this call's barrier
+};
+
+// Balanced split of n items over B parts: [begin, end) of part b.
+__host__ __device__ __forceinline__ void split_range(int n, int b, int B, int& begin,
+                                                     int& end) {
+  const int base = n / B, rem = n % B;
+  begin = b * base + (b < rem ? b : rem);
+  end = begin + base + (b < rem ? 1 : 0);
+}
+
+// Chunks of 32 groups per lane for a K-long row: K < 1024 -> 1 (lanes past
+// K/32 idle); else K / 1024 when that is an instantiated count; 0 otherwise.
+__host__ __device__ inline int chunks_per_lane(int K) {
+  if (K % 32 != 0) return 0;
+  if (K < 1024) return 1;
+  if (K % 1024 != 0) return 0;
+  const int c = K / 1024;
+  return (c == 1 || c == 2 || c == 4 || c == 6 || c == 8) ? c : 0;
+}
+
+// fp32 reciprocal root of one token's RMSNorm, reduced by the first 8 warps
+// of the CTA (warp = segment) in the fixed fp64 order; valid in rf after the
+// caller's __syncthreads.  dseg: 8 doubles of shared memory.
+__device__ inline void rms_partial(const DecArgs& a, int t, double* dseg) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kRouterWarps) return;
+  const int H = a.sh.H, L = H / kSeg, chunks = L / 4;
+  const size_t base = static_cast<size_t>(t) * H + static_cast<size_t>(warp) * L;
+  double acc = 0.0;
+  for (int c = lane; c < chunks; c += 32) {
+    const float4 v = load_x4(a.x, a.dt, base + 4 * c);
+    acc = __fma_rn(static_cast<double>(v.x), static_cast<double>(v.x), acc);
+    acc = __fma_rn(static_cast<double>(v.y), static_cast<double>(v.y), acc);
+    acc = __fma_rn(static_cast<double>(v.z), static_cast<double>(v.z), acc);
+    acc = __fma_rn(static_cast<double>(v.w), static_cast<double>(v.w), acc);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) acc = __dadd_rn(acc, __shfl_down_sync(0xffffffffu, acc, d));
+  if (lane == 0) dseg[warp] = acc;
+}
+
+__device__ inline float rms_finish(const DecArgs& a, const double* dseg) {
+  double a0 = __dadd_rn(dseg[0], dseg[4]), a1 = __dadd_rn(dseg[1], dseg[5]);
+  double a2 = __dadd_rn(dseg[2], dseg[6]), a3 = __dadd_rn(dseg[3], dseg[7]);
+  a0 = __dadd_rn(a0, a2);
+  a1 = __dadd_rn(a1, a3);
+  const double mean = __ddiv_rn(__dadd_rn(a0, a1), static_cast<double>(a.sh.H));
+  return __double2float_rn(
+      __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(mean, static_cast<double>(a.eps)))));
+}
+
+// x_hat for elements idx..idx+3 of token t (x row offset included in idx).
+__device__ __forceinline__ float4 xhat4(const DecArgs& a, size_t idx, int k, float rf) {
+  float4 v = load_x4(a.x, a.dt, idx);
+  if (a.gamma != nullptr) {
+    const float4 g = __ldg(reinterpret_cast<const float4*>(a.gamma + k));
+    v.x = __fmul_rn(__fmul_rn(v.x, rf), g.x);
+    v.y = __fmul_rn(__fmul_rn(v.y, rf), g.y);
+    v.z = __fmul_rn(__fmul_rn(v.z, rf), g.z);
+    v.w = __fmul_rn(__fmul_rn(v.w, rf), g.w);
+  }
+  return v;
+}
+
+// Stores x_hat[k..k+3] (k % 4 == 0) pre-scaled into the swizzled layout.
+__device__ __forceinline__ void swz_store4(float* dst, int k, float4 v) {
+  const int g = k >> 5, i = k & 31;
+  v.x *= swz_prescale(i);
+  v.y *= swz_prescale(i + 1);
+  v.z *= swz_prescale(i + 2);
+  v.w *= swz_prescale(i + 3);
+  *reinterpret_cast<float4*>(dst + swz_index(g, i)) = v;
+}
+
+// The routing plan of the call, one selected expert ("slot") per lane.
+struct LanePlan {
+  int n_act;       // slots (distinct experts), warp-uniform
+  int e;           // expert of slot `lane` (lane < n_act)
+  int p0;          // first plan position of the slot
+  int n;           // entries of the slot
+  unsigned tmask;  // tokens of the slot (bit t)
+};
+
+template <int EPL>
+__device__ __forceinline__ void select_token(const DecArgs& a, int t, int& id, float& w) {
+  const size_t o = static_cast<size_t>(t) * a.sh.E;
+  warp_select_regs<EPL>(a.ws.skey + o, a.ws.sval + o, a.sh, id, w);
+}
+
+// Every warp derives the selection of the call's T tokens from the
+// published scores (bit-identical in every warp), then the plan: entries
+// i = t*k + j grouped by expert ascending, ascending i inside an expert.
+// With `publish`, the plan is also written to the workspace.
+static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, bool publish,
+                                             LanePlan& lp) {
+  const int lane = threadIdx.x & 31;
+  const int k = a.sh.k, T = a.T, N = T * k;
+  int my_id = 0;
+  float my_w = 0.0f;
+  for (int t = 0; t < T; ++t) {
+    int id;
+    float w;
+    switch (epl) {
+      case 1: select_token<1>(a, t, id, w); break;
+      case 2: select_token<2>(a, t, id, w); break;
+      case 4: select_token<4>(a, t, id, w); break;
+      default: select_token<8>(a, t, id, w); break;
+    }
+    const int src = lane - t * k;
+    const int sid = __shfl_sync(0xffffffffu, id, src & 31);
+    const float sw = __shfl_sync(0xffffffffu, w, src & 31);
+    if (src >= 0 && src < k) {
+      my_id = sid;
+      my_w = sw;
+    }
+  }
+  const bool valid = lane < N;
+  const int e = valid ? my_id : 0x40000000 + lane;  // distinct dummies
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned grp = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(grp & lt), cnt = __popc(grp);
+  const bool leader = valid && (grp & lt) == 0;
+  const unsigned leaders = __ballot_sync(0xffffffffu, leader);
+  int before = 0, base = 0;
+  for (unsigned m = leaders; m; m &= m - 1) {
+    const int l = __ffs(m) - 1;
+    const int el = __shfl_sync(0xffffffffu, e, l);
+    const int cl = __shfl_sync(0xffffffffu, cnt, l);
+    if (el < e) {
+      ++before;
+      base += cl;
+    }
+  }
+  unsigned tmask = 0;
+  for (unsigned m = grp; m; m &= m - 1) tmask |= 1u << ((__ffs(m) - 1) / k);
+  lp.n_act = __popc(leaders);
+  lp.e = 0;
+  lp.p0 = 0;
+  lp.n = 0;
+  lp.tmask = 0;
+  for (unsigned m = leaders; m; m &= m - 1) {
+    const int l = __ffs(m) - 1;
+    const int al = __shfl_sync(0xffffffffu, before, l);
+    const int el = __shfl_sync(0xffffffffu, e, l);
+    const int bl = __shfl_sync(0xffffffffu, base, l);
+    const int cl = __shfl_sync(0xffffffffu, cnt, l);
+    const unsigned tl = __shfl_sync(0xffffffffu, tmask, l);
+    if (lane == al) {
+      lp.e = el;
+      lp.p0 = bl;
+      lp.n = cl;
+      lp.tmask = tl;
+    }
+  }
+  if (publish) {
+    const Workspace& ws = a.ws;
+    if (valid) {
+      const int p = base + rank;
+      ws.ids[lane] = my_id;
+      ws.topw[lane] = my_w;
+      ws.perm[p] = lane;
+      ws.inv[lane] = p;
+    }
+    if (lane < lp.n_act) {
+      ws.active[lane] = lp.e;
+      ws.dslot[lane] = lp.e;
+      ws.dslot[32 + lane] = lp.p0;
+      ws.dslot[64 + lane] = lp.n;
+    }
+    if (lane == 0) *ws.n_active = lp.n_act;
+  }
+}
+
+// ---- host side ------------------------------------------------------------
+
+// Launch with cudaLaunchKernelEx: optional programmatic stream serialisation
+// (the kernel may start while the previous one finishes; it waits with
+// griddepcontrol.wait) and optional cooperative launch (all CTAs resident).
+template <typename K>
+cudaError_t launch_k(K kernel, int grid, int threads, size_t smem, cudaStream_t s,
+                     const DecArgs& a, bool pdl, bool coop) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <typename K>
+cudaError_t set_smem_once(K kernel, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem));
+}
+
+// Configurations of the two kernels (the .cu files instantiate these).
+constexpr int kStagesB1 = 2, kWarpsB1 = 12;  // dec_ab, one token
+constexpr int kStagesB4 = 2, kWarpsB4 = 8;   // dec_ab, up to four tokens
+constexpr int kStagesC = 3, kWarpsC = 8;     // dec_c
+
+// Bytes of dynamic shared memory of dec_ab for a shape and NT.
+__host__ __device__ inline size_t ab_smem_bytes(const Shape& sh, int NT, int warps, int stages,
+                                                int n_sm) {
+  const int L = (sh.E + n_sm - 1) / n_sm;
+  size_t b = static_cast<size_t>(NT) * swz_pad(sh.H) * 4;              // xs
+  b += static_cast<size_t>(warps) * stages * (sh.H + sh.H / 8);        // rings
+  b += static_cast<size_t>(warps) * stages * 8;                        // mbarriers
+  b += static_cast<size_t>(L) * kRouterWarps * NT * 4;                 // logit segments
+  b += 8 * 8 + 16;                                                     // fp64 partials, rf
+  return b;
+}
+
+__host__ __device__ inline size_t c_ring_bytes(const Shape& sh, int warps, int stages) {
+  return static_cast<size_t>(warps) * stages * kRowsC * (sh.I / 2 + sh.I / 16);
+}
+
+__host__ __device__ inline size_t c_h_bytes(const Shape& sh, int T, int hstride) {
+  return static_cast<size_t>(T * sh.k + T) * hstride * 4;
+}
+
+__host__ __device__ inline size_t c_smem_bytes(const Shape& sh, int T, int NT, bool h_smem,
+                                               int hstride) {
+  size_t b = c_ring_bytes(sh, kWarpsC, kStagesC);
+  b += static_cast<size_t>(kWarpsC) * kStagesC * 8 + 16;             // mbarriers (+h barrier)
+  b += static_cast<size_t>(kWarpsC) * 2 * kRowsC * NT * 4;           // partial rows
+  if (h_smem) b += c_h_bytes(sh, T, hstride);
+  return b;
+}
+
+cudaError_t launch_dec_ab(const DecArgs& a, int NT, int cpl, size_t smem, int n_sm,
+                          cudaStream_t s);
+cudaError_t launch_dec_c(const DecArgs& a, int NT, int cpl, bool h_smem, size_t smem, int n_sm,
+                         bool pdl, cudaStream_t s);
+
+}  // namespace dec
+}  // namespace moe

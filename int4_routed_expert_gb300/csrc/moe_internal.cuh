@@ -1,0 +1,116 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Per-handle device workspace, carved out of one cudaMalloc at create time.
+struct Workspace {
+  float* xf;         // [Tm][H]      fp32 copy (or RMSNorm) of the input
+  float* logits;     // [Tm][E]
+  int32_t* ids;      // [Tm][k]
+  float* topw;       // [Tm][k]
+  int32_t* counts;   // [E]
+  int32_t* offsets;  // [E+1]
+  int32_t* perm;     // [Tm*k]
+  int32_t* inv;      // [Tm*k]  position of entry i inside perm
+  int32_t* active;   // [E]
+  int32_t* n_active; // [1]
+  float* hbuf;       // [Tm*k + Tm][hstride] SwiGLU activations (routed, then shared)
+  float* obuf;       // [Tm*k + Tm][H]       expert outputs before the combine
+  float* sval;       // [Tm][E] un-biased router scores (small-batch path)
+  float* skey;       // [Tm][E] selection keys s + bias (small-batch path)
+  int32_t* dev_err;  // device error word (bounded waits that gave up)
+  int32_t* dslot;    // [3][32] small-batch slot table: expert, first position, entries
+  unsigned long long* gbar;  // grid barrier counter of the small-batch kernel (monotonic)
+  int hstride;       // row stride of hbuf in floats (>= Imax, multiple of 1024)
+};
+
+struct Shape {
+  int H, I, Is, E, k, n_group, topk_group, n_shared;
+  float rsf;
+};
+
+}  // namespace moe
+
+// Phase ids of the trace API (a call records only the phases it runs).
+#define MOE_N_PHASES 10
+
+struct moe_layer {
+  moe_config_t cfg;
+  moe_weights_t w;
+  moe::Shape sh;
+  void* ws_base;
+  size_t ws_bytes;
+  moe::Workspace ws;
+  int device;
+  char err[512];
+  int n_sm;
+  unsigned long long decode_calls;  // small-batch launches so far (grid barrier targets)
+  // phase tracing: trace_cap calls x (MOE_N_PHASES + 1) events, and per call
+  // the phase id recorded after each launched phase
+  cudaEvent_t* trace_ev;
+  int* trace_phase;  // [trace_cap][MOE_N_PHASES]
+  int* trace_nrec;   // [trace_cap]
+  int trace_cap;
+  int trace_used;
+};
+
+namespace moe {
+
+// ---- launchers (each returns the cudaError_t of its launch) --------------
+
+// x (fp32 or bf16) -> xf fp32, optionally RMSNorm'd with gamma (fp64 sum of
+// squares in the fixed order of the router).
+cudaError_t launch_prep(const void* x, moe_dtype_t dtype, int T, int H,
+                        const float* gamma, float eps, float* xf, cudaStream_t s);
+
+// logits[t][e] = x_t . Wr_e in the fixed summation order.
+cudaError_t launch_router_logits(const float* xf, int T, int H, const float* Wr, int E,
+                                 float* logits, cudaStream_t s);
+
+// warp-per-token noaux_tc selection -> ids, topw.
+cudaError_t launch_select(const float* logits, const float* bias, int T, const Shape& sh,
+                          int32_t* ids, float* topw, cudaStream_t s);
+
+// single-CTA stable routing plan.
+cudaError_t launch_plan(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                        int32_t* n_active, cudaStream_t s);
+
+// SwiGLU gate/up projections over the plan (+ shared expert): hbuf.
+cudaError_t launch_gate_up(const moe_weights_t& w, const Shape& sh, int T,
+                           const Workspace& ws, cudaStream_t s);
+
+// down projection over the plan (+ shared expert): obuf.
+cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T,
+                        const Workspace& ws, cudaStream_t s);
+
+// y = (acc ? y : 0) + sum_j w_tj * o_(t,j) + o_shared_t.
+cudaError_t launch_combine(const Shape& sh, int T, const Workspace& ws, float* y,
+                           int accumulate, cudaStream_t s);
+
+// Fused small-batch path (T <= 4, T*k <= 32).  When `marker.fn` is set
+// (phase tracing), the kernels are launched without the programmatic-
+// dependency overlap and marker.fn(ctx, phase) is called after each of them.
+struct PhaseMarker {
+  void (*fn)(void* ctx, int phase);
+  void* ctx;
+  void mark(int phase) const {
+    if (fn) fn(ctx, phase);
+  }
+};
+bool decode_path_ok(const Shape& sh, int T, int n_sm);
+// calls: the handle's count of small-batch launches (read and advanced).
+cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const void* x,
+                          moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,
+                          float* y, int accumulate, int n_sm, unsigned long long* calls,
+                          const PhaseMarker& pm, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,258 @@
+"""ctypes binding of libmoe.so, with the C ABI's names (argument marshalling only).
+
+Every step of the layer runs in the library's CUDA kernels.  If the library
+is missing or cannot be loaded, ``load`` raises; there is no Python or CPU
+fallback.
+
+Low-level functions mirror include/moe.h one to one:
+    moe_layer_create, moe_route, moe_forward, moe_destroy, moe_last_error,
+    moe_workspace_bytes, moe_trace_enable, moe_trace_read,
+    moe_trace_phase_name, moe_device_status
+``MoELayer`` wraps a handle around torch tensors (device memory and streams
+only) for the tests and the benchmark.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_CAPACITY = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_OOM = -5
+MOE_F32 = 0
+MOE_BF16 = 1
+
+_STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
+           -3: "MOE_ERR_CAPACITY", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_OOM"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class moe_config_t(C.Structure):
+    _fields_ = [("hidden", C.c_int), ("inter", C.c_int), ("n_experts", C.c_int),
+                ("top_k", C.c_int), ("n_group", C.c_int), ("topk_group", C.c_int),
+                ("routed_scaling_factor", C.c_float), ("n_shared", C.c_int),
+                ("shared_inter", C.c_int), ("group_size", C.c_int),
+                ("max_tokens", C.c_int)]
+
+
+class moe_weights_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "router_w", "router_bias", "gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
+        "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")]
+
+
+class moe_plan_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "topk_ids", "topk_w", "counts", "offsets", "perm", "active", "n_active")]
+
+
+EXPORTED = ("moe_layer_create", "moe_route", "moe_forward", "moe_destroy",
+            "moe_last_error", "moe_workspace_bytes", "moe_trace_enable", "moe_trace_read",
+            "moe_trace_phase_name", "moe_device_status")
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Load libmoe.so (build it first with int4_routed_expert_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: run `python -m int4_routed_expert_gb300.build` "
+                          "(there is no fallback implementation)")
+    L = C.CDLL(path)
+    L.moe_layer_create.restype = C.c_int
+    L.moe_layer_create.argtypes = [C.POINTER(moe_config_t), C.POINTER(moe_weights_t),
+                                   C.POINTER(C.c_void_p)]
+    L.moe_route.restype = C.c_int
+    L.moe_route.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_float,
+                            C.POINTER(moe_plan_t), C.c_void_p]
+    L.moe_forward.restype = C.c_int
+    L.moe_forward.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
+                              C.c_void_p, C.c_float, C.c_int, C.POINTER(moe_plan_t),
+                              C.c_void_p]
+    L.moe_destroy.restype = None
+    L.moe_destroy.argtypes = [C.c_void_p]
+    L.moe_last_error.restype = C.c_char_p
+    L.moe_last_error.argtypes = [C.c_void_p]
+    L.moe_workspace_bytes.restype = C.c_size_t
+    L.moe_workspace_bytes.argtypes = [C.POINTER(moe_config_t)]
+    L.moe_trace_enable.restype = C.c_int
+    L.moe_trace_enable.argtypes = [C.c_void_p, C.c_int]
+    L.moe_trace_read.restype = C.c_int
+    L.moe_trace_read.argtypes = [C.c_void_p, C.POINTER(C.c_float), C.c_int,
+                                 C.POINTER(C.c_int), C.POINTER(C.c_int)]
+    L.moe_trace_phase_name.restype = C.c_char_p
+    L.moe_trace_phase_name.argtypes = [C.c_int]
+    L.moe_device_status.restype = C.c_int
+    L.moe_device_status.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
+    _lib = L
+    return L
+
+
+def moe_last_error(h) -> str:
+    return (load().moe_last_error(h) or b"").decode()
+
+
+def _check(st: int, h=None):
+    if st != MOE_OK:
+        raise MoeError(st, moe_last_error(h))
+
+
+def moe_workspace_bytes(cfg: moe_config_t) -> int:
+    return int(load().moe_workspace_bytes(C.byref(cfg)))
+
+
+def moe_layer_create(cfg: moe_config_t, w: moe_weights_t) -> C.c_void_p:
+    h = C.c_void_p()
+    _check(load().moe_layer_create(C.byref(cfg), C.byref(w), C.byref(h)), None)
+    return h
+
+
+def moe_route(h, x: int, dtype: int, T: int, gamma: int | None, eps: float,
+              plan: moe_plan_t | None, stream: int | None) -> None:
+    _check(load().moe_route(h, x, dtype, T, gamma, eps,
+                            C.byref(plan) if plan is not None else None, stream), h)
+
+
+def moe_forward(h, x: int, dtype: int, T: int, y: int, gamma: int | None, eps: float,
+                accumulate: int, plan: moe_plan_t | None, stream: int | None) -> None:
+    _check(load().moe_forward(h, x, dtype, T, y, gamma, eps, accumulate,
+                              C.byref(plan) if plan is not None else None, stream), h)
+
+
+def moe_destroy(h) -> None:
+    if h:
+        load().moe_destroy(h)
+
+
+def moe_trace_enable(h, n_calls: int) -> None:
+    _check(load().moe_trace_enable(h, n_calls), h)
+
+
+def moe_trace_phase_name(p: int) -> str | None:
+    r = load().moe_trace_phase_name(p)
+    return r.decode() if r else None
+
+
+def moe_device_status(h) -> int:
+    """Device error flags of the handle (0 = fine); raises MoeError if set."""
+    f = C.c_int32(0)
+    _check(load().moe_device_status(h, C.byref(f)), h)
+    return f.value
+
+
+def moe_trace_read(h, cap: int):
+    """-> (phase names, list of per-call lists of phase milliseconds)."""
+    buf = (C.c_float * max(1, cap * 16))()
+    n, npha = C.c_int(), C.c_int()
+    _check(load().moe_trace_read(h, buf, cap, C.byref(n), C.byref(npha)), h)
+    names = [moe_trace_phase_name(p) for p in range(npha.value)]
+    rows = [[buf[c * npha.value + p] for p in range(npha.value)] for c in range(n.value)]
+    return names, rows
+
+
+# ---------------------------------------------------------- torch wrapper --
+
+def config_for(shape, max_tokens: int) -> moe_config_t:
+    return moe_config_t(shape.hidden, shape.inter, shape.n_experts, shape.top_k,
+                        shape.n_group, shape.topk_group, shape.routed_scaling_factor,
+                        shape.n_shared, shape.i_shared if shape.n_shared else 0,
+                        shape.group_size, max_tokens)
+
+
+def weights_for(L) -> moe_weights_t:
+    """moe_weights_t from a workloads.gen.LayerInputs living on the device."""
+    p = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    return moe_weights_t(p(L.router_w), p(L.router_b), p(L.gate_q), p(L.gate_s), p(L.up_q),
+                         p(L.up_s), p(L.down_q), p(L.down_s), p(L.sh_gate_q), p(L.sh_gate_s),
+                         p(L.sh_up_q), p(L.sh_up_s), p(L.sh_down_q), p(L.sh_down_s))
+
+
+class Plan:
+    """Device buffers for the routing outputs of T tokens."""
+
+    def __init__(self, T: int, k: int, E: int, device):
+        import torch
+        i32 = dict(dtype=torch.int32, device=device)
+        self.topk_ids = torch.empty(T, k, **i32)
+        self.topk_w = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.perm = torch.empty(T * k, **i32)
+        self.active = torch.full((E,), -1, **i32)
+        self.n_active = torch.empty(1, **i32)
+
+    def c(self) -> moe_plan_t:
+        return moe_plan_t(*(getattr(self, n).data_ptr() for n, _ in moe_plan_t._fields_))
+
+
+class MoELayer:
+    """Handle + the tensors it borrows.  torch supplies memory and streams."""
+
+    def __init__(self, layer_inputs, max_tokens: int):
+        self.inputs = layer_inputs  # keeps the weights alive
+        self.shape = layer_inputs.shape
+        self.max_tokens = max_tokens
+        self.cfg = config_for(self.shape, max_tokens)
+        self.h = moe_layer_create(self.cfg, weights_for(layer_inputs))
+
+    def close(self):
+        if self.h:
+            moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _dtype(x) -> int:
+        import torch
+        if x.dtype == torch.float32:
+            return MOE_F32
+        if x.dtype == torch.bfloat16:
+            return MOE_BF16
+        raise TypeError(f"x must be fp32 or bf16, got {x.dtype}")
+
+    @staticmethod
+    def _stream(stream) -> int:
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return s.cuda_stream
+
+    def route(self, x, gamma=None, eps: float = 1e-5, plan: Plan | None = None,
+              stream=None) -> Plan:
+        T = x.shape[0]
+        plan = plan or Plan(T, self.shape.top_k, self.shape.n_experts, x.device)
+        pc = plan.c()
+        moe_route(self.h, x.data_ptr(), self._dtype(x), T,
+                  gamma.data_ptr() if gamma is not None else None, eps, pc,
+                  self._stream(stream))
+        return plan
+
+    def forward(self, x, y=None, gamma=None, eps: float = 1e-5, accumulate: bool = False,
+                plan: Plan | None = None, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=x.device)
+        pc = plan.c() if plan is not None else None
+        moe_forward(self.h, x.data_ptr(), self._dtype(x), T, y.data_ptr(),
+                    gamma.data_ptr() if gamma is not None else None, eps,
+                    1 if accumulate else 0, pc, self._stream(stream))
+        return y

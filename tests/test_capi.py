@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports what
+include/moe.h declares, and argument validation happens before any CUDA
+call.  None of these launch a kernel, so they run without a GPU."""
+from __future__ import annotations
+
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    from int4_routed_expert_gb300 import build as b
+    b.build()
+    import int4_routed_expert_gb300 as mod
+    mod.load()
+    return mod
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for mt in re.finditer(r"\b(moe_[a-z_]+)\s*\(", text):
+            names.add(mt.group(1))
+    return names
+
+
+def _cfg(m, **kw):
+    c = dict(hidden=256, inter=128, n_experts=16, top_k=4, n_group=4, topk_group=2,
+             routed_scaling_factor=2.5, n_shared=1, shared_inter=128, group_size=32,
+             max_tokens=8)
+    c.update(kw)
+    return m.moe.moe_config_t(**c)
+
+
+def _fake_weights(m, base=0x10000000, step=0x100000):
+    return m.moe.moe_weights_t(*[base + i * step for i in range(14)])
+
+
+def test_library_builds_and_loads(m):
+    assert os.path.exists(m.moe.LIB_PATH)
+
+
+def test_every_declared_symbol_is_exported(m):
+    lib = m.load()
+    names = _declared()
+    assert {"moe_layer_create", "moe_route", "moe_forward", "moe_destroy"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(m.EXPORTED) <= names
+
+
+def test_workspace_bytes(m):
+    small = m.moe_workspace_bytes(_cfg(m))
+    big = m.moe_workspace_bytes(_cfg(m, max_tokens=64))
+    assert 0 < small < big
+    assert m.moe_workspace_bytes(_cfg(m, group_size=64)) == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(hidden=300), dict(hidden=128), dict(inter=100), dict(n_experts=0),
+    dict(n_experts=2048), dict(n_group=3), dict(topk_group=5), dict(top_k=0),
+    dict(top_k=33), dict(top_k=9, topk_group=2), dict(group_size=64), dict(max_tokens=0),
+    dict(n_shared=2), dict(shared_inter=100), dict(routed_scaling_factor=float("nan")),
+])
+def test_bad_configs_are_unsupported(m, bad):
+    h = C.c_void_p()
+    st = m.load().moe_layer_create(C.byref(_cfg(m, **bad)), C.byref(_fake_weights(m)), C.byref(h))
+    assert st == -2 and not h.value
+    assert m.moe_last_error(None)
+
+
+def test_null_or_misaligned_weights(m):
+    lib = m.load()
+    w = _fake_weights(m)
+    w.gate_q = None
+    h = C.c_void_p()
+    assert lib.moe_layer_create(C.byref(_cfg(m)), C.byref(w), C.byref(h)) == -1
+    w = _fake_weights(m)
+    w.down_s = 0x10000008
+    assert lib.moe_layer_create(C.byref(_cfg(m)), C.byref(w), C.byref(h)) == -1
+    # shared pointers may be NULL without a shared expert
+    w = _fake_weights(m)
+    w.sh_gate_q = None
+    assert lib.moe_layer_create(C.byref(_cfg(m)), C.byref(w), C.byref(h)) == -1
+
+
+def test_create_without_gpu_fails_loudly(m):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = C.c_void_p()
+    st = m.load().moe_layer_create(C.byref(_cfg(m)), C.byref(_fake_weights(m)), C.byref(h))
+    assert st == -4 and not h.value  # MOE_ERR_CUDA: there is no CPU fallback
+
+
+def test_null_handle(m):
+    lib = m.load()
+    assert lib.moe_forward(None, None, 0, 1, None, None, 0.0, 0, None, None) == -1
+    assert lib.moe_route(None, None, 0, 1, None, 0.0, None, None) == -1
+    assert lib.moe_trace_enable(None, 1) == -1
+    flags = C.c_int32()
+    assert lib.moe_device_status(None, C.byref(flags)) == -1
+    lib.moe_destroy(None)
+
+
+def test_phase_names(m):
+    names = [m.moe_trace_phase_name(p) for p in range(10)]
+    assert all(names) and len(set(names)) == 10
+    assert m.moe_trace_phase_name(10) is None and m.moe_trace_phase_name(-1) is None
+
+
+def test_binding_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "int4_routed_expert_gb300")
+    for path in glob.glob(os.path.join(pkg, "*.py")) + glob.glob(os.path.join(pkg, "csrc", "*")):
+        text = open(path, errors="replace").read()
+        assert not re.search(r"^\s*(import|from)\s+(oracle|numpy)\b", text, re.M), path
+        assert "liboracle" not in text and "oracle.cpp" not in text, path

@@ -1,0 +1,320 @@
+"""Parity of the CUDA layer, called through the C ABI, with the CPU oracle.
+
+Expert ids, gate weights and the whole routing plan must match bit for bit;
+layer outputs must match within TOL (per-token max abs error / max abs
+oracle output) of the fp32-accumulated oracle.  Every input is seeded and
+synthetic (workloads/).  Runs only on a machine with a CUDA GPU.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import RMS_EPS, TOL, oracle_layer, rel_err_per_token, router_of
+from workloads import CONFIGS
+from workloads.configs import LayerShape, Workload
+from workloads.gen import HostExpertCache, gen_activations, gen_layer, gen_norm_weight
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_routed_expert_gb300 import build as b
+    b.build()
+    import int4_routed_expert_gb300 as mod
+    mod.load()
+    return mod
+
+
+def _check_plan(plan, ids_o, E):
+    P = oracle.plan(ids_o, E)
+    assert np.array_equal(plan.counts.cpu().numpy(), P["counts"])
+    assert np.array_equal(plan.offsets.cpu().numpy(), P["offsets"])
+    assert np.array_equal(plan.perm.cpu().numpy(), P["perm"])
+    n = int(plan.n_active.cpu().numpy()[0])
+    assert n == P["n_active"]
+    assert np.array_equal(plan.active.cpu().numpy()[:n], P["active"])
+
+
+def _run_full(m, wl, L, x_cpu, *, layer=0, sample=None, gamma=None, max_tokens=None,
+              tol=TOL, cache=None, handle=None):
+    """Forward x on the GPU with a plan; compare routing bit for bit and y."""
+    sh = wl.shape
+    T = x_cpu.shape[0]
+    own = handle is None
+    h = handle or m.MoELayer(L, max_tokens or T)
+    x = x_cpu.to(DEV)
+    g = gamma.to(DEV) if gamma is not None else None
+    plan = m.Plan(T, sh.top_k, sh.n_experts, DEV)
+    y = h.forward(x, gamma=g, eps=RMS_EPS, plan=plan)
+    torch.cuda.synchronize()
+    assert m.moe_device_status(h.h) == 0
+    x32 = x_cpu.float().numpy()
+    eps = RMS_EPS if gamma is not None else 0.0
+    gnp = gamma.numpy() if gamma is not None else None
+    router = router_of(wl, layer)
+    _, _, ids_o, w_o = oracle.route(sh, router[0], router[1], x32, eps, gnp)
+    ids = plan.topk_ids.cpu().numpy()
+    wts = plan.topk_w.cpu().numpy()
+    assert np.array_equal(ids, ids_o), (ids, ids_o)
+    assert np.array_equal(wts.view(np.uint32), w_o.view(np.uint32))
+    _check_plan(plan, ids_o, sh.n_experts)
+    tokens = list(range(T)) if sample is None else [t for t in sample if t < T]
+    y_o, _, _, _ = oracle_layer(wl, layer, router, x32, tokens, eps=eps, gamma=gnp, cache=cache)
+    err = rel_err_per_token(y.cpu().numpy()[tokens], y_o)
+    assert err.max() <= tol, err
+    if own:
+        h.close()
+    return y, plan, err
+
+
+# ------------------------------------------------------------------ tiny layer
+
+@pytest.mark.parametrize("T", [1, 2, 3, 17, 64, 100])
+def test_tiny_layer(m, T):
+    wl = CONFIGS["tiny"]
+    L = gen_layer(wl, device=DEV)
+    x = gen_activations(wl, T, call=T)
+    _run_full(m, wl, L, x, tol=1e-4)
+
+
+# ------------------------------------------------------------- shape sweep ---
+
+SHAPES = [
+    # H, I, E, k, n_group, topk_group, n_shared  (I % 256 == 0 and E <= 256 with
+    # E = 32 * 2^j take the fused small-batch path for T <= 4)
+    (256, 256, 32, 4, 4, 2, 1),
+    (512, 512, 64, 6, 8, 3, 1),
+    (1024, 256, 128, 8, 8, 4, 1),
+    (2048, 1024, 256, 8, 8, 4, 1),
+    (1024, 512, 64, 4, 2, 1, 0),
+    (256, 256, 32, 4, 32, 8, 1),    # one expert per group
+    (768, 96, 27, 5, 9, 3, 1),      # general path only
+    (256, 128, 1024, 8, 8, 4, 1),   # 1024 experts
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("T", [1, 3, 4, 9])
+def test_shape_sweep(m, shape, T):
+    H, I, E, k, ng, tg, ns = shape
+    sh = LayerShape(H, I, E, k, ng, tg, 1.5, n_shared=ns)
+    wl = Workload("sweep", sh, T, 1, "bf16" if T % 2 else "f32", "uniform",
+                  7000 + H + I + E + k)
+    L = gen_layer(wl, device=DEV)
+    x = gen_activations(wl, T, call=0)
+    _run_full(m, wl, L, x, max_tokens=max(T, 16))
+
+
+def test_small_batch_with_rmsnorm(m):
+    sh = LayerShape(1024, 512, 64, 6, 8, 3, 2.0)
+    wl = Workload("norm", sh, 2, 1, "f32", "zipf", 7101, rmsnorm_eps=1e-5)
+    L = gen_layer(wl, device=DEV)
+    for T in (1, 2, 4):
+        x = gen_activations(wl, T, call=T) * 3.0
+        _run_full(m, wl, L, x, gamma=gen_norm_weight(wl, 0), max_tokens=8)
+
+
+# -------------------------------------------------------- API behaviour ------
+
+def _tiny_handle(m, max_tokens=8):
+    wl = CONFIGS["tiny"]
+    L = gen_layer(wl, device=DEV)
+    return wl, L, m.MoELayer(L, max_tokens)
+
+
+def test_device_status_clean(m):
+    wl, L, h = _tiny_handle(m)
+    h.forward(gen_activations(wl, 2, call=1).to(DEV))
+    torch.cuda.synchronize()
+    assert m.moe_device_status(h.h) == 0
+    h.close()
+
+
+def test_zero_tokens_is_noop(m):
+    wl, L, h = _tiny_handle(m)
+    x = torch.zeros(0, wl.shape.hidden, device=DEV)
+    y = torch.full((1, wl.shape.hidden), 7.0, device=DEV)
+    m.moe_forward(h.h, x.data_ptr() if x.numel() else y.data_ptr(), m.MOE_F32, 0,
+                  y.data_ptr(), None, 0.0, 0, None, None)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+    h.close()
+
+
+def test_capacity_and_argument_errors(m):
+    wl, L, h = _tiny_handle(m, max_tokens=4)
+    H = wl.shape.hidden
+    x = torch.randn(5, H, device=DEV)
+    with pytest.raises(m.MoeError) as ei:
+        h.forward(x)
+    assert ei.value.status == -3
+    buf = torch.zeros(4 * H + 4, device=DEV)
+    with pytest.raises(m.MoeError) as ei:  # misaligned x
+        m.moe_forward(h.h, buf.data_ptr() + 4, m.MOE_F32, 1, buf.data_ptr() + 4 * H * 2,
+                      None, 0.0, 0, None, None)
+    assert ei.value.status == -1
+    xx = torch.randn(2, H, device=DEV)
+    with pytest.raises(m.MoeError) as ei:  # overlap outside the residual form
+        m.moe_forward(h.h, xx.data_ptr(), m.MOE_F32, 2, xx.data_ptr(), None, 0.0, 1, None, None)
+    assert ei.value.status == -1
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_forward(h.h, xx.data_ptr(), 7, 2, buf.data_ptr(), None, 0.0, 0, None, None)
+    assert ei.value.status == -1
+    h.close()
+
+
+def test_deterministic_repeat(m):
+    sh = LayerShape(1024, 512, 64, 6, 8, 3, 2.0)
+    wl = Workload("det", sh, 4, 1, "bf16", "zipf", 7202)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 64)
+    for T in (1, 4, 33):
+        x = gen_activations(wl, T, call=T).to(DEV)
+        y1 = h.forward(x).clone()
+        y2 = h.forward(x).clone()
+        assert torch.equal(y1, y2)
+    h.close()
+
+
+def test_route_matches_forward_plan(m):
+    sh = LayerShape(512, 512, 64, 6, 8, 3, 2.0)
+    wl = Workload("route", sh, 4, 1, "bf16", "zipf", 7303)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 64)
+    for T in (1, 3, 40):
+        x = gen_activations(wl, T, call=T).to(DEV)
+        p1 = h.route(x)
+        p2 = m.Plan(T, sh.top_k, sh.n_experts, DEV)
+        h.forward(x, plan=p2)
+        torch.cuda.synchronize()
+        for name in ("topk_ids", "topk_w", "counts", "offsets", "perm", "n_active"):
+            assert torch.equal(getattr(p1, name), getattr(p2, name)), name
+        n = int(p1.n_active.item())
+        assert torch.equal(p1.active[:n], p2.active[:n])
+    h.close()
+
+
+def test_residual_in_place(m):
+    for sh in (CONFIGS["tiny"].shape, LayerShape(1024, 512, 64, 6, 8, 3, 2.0)):
+        wl = Workload("resid", sh, 3, 1, "f32", "zipf", 7404, rmsnorm_eps=1e-5)
+        L = gen_layer(wl, device=DEV)
+        h = m.MoELayer(L, 8)
+        gamma = gen_norm_weight(wl, 0)
+        for T in (1, 3, 6):
+            x0 = (gen_activations(wl, T, call=T) * 2.0).float()
+            xd = x0.to(DEV)
+            h.forward(xd, y=xd, gamma=gamma.to(DEV), eps=RMS_EPS, accumulate=True)
+            torch.cuda.synchronize()
+            y_o, _, _, _ = oracle_layer(wl, 0, router_of(wl), x0.numpy(), range(T), eps=RMS_EPS,
+                                        gamma=gamma.numpy(), resid=x0.numpy())
+            err = rel_err_per_token(xd.cpu().numpy() - x0.numpy(), y_o - x0.numpy())
+            assert err.max() <= TOL
+        h.close()
+
+
+def test_trace_phases(m):
+    sh = LayerShape(1024, 512, 64, 6, 8, 3, 2.0)
+    wl = Workload("trace", sh, 4, 1, "bf16", "zipf", 7505)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 64)
+    m.moe_trace_enable(h.h, 3)
+    h.forward(gen_activations(wl, 1, call=0).to(DEV))
+    h.forward(gen_activations(wl, 20, call=1).to(DEV))
+    names, rows = m.moe_trace_read(h.h, 3)
+    assert len(rows) == 2 and len(names) == 10
+    small = {n for n, v in zip(names, rows[0]) if v > 0}
+    general = {n for n, v in zip(names, rows[1]) if v > 0}
+    assert small == {"decode_router_gate_up", "decode_down_combine"}
+    assert {"prep", "router_logits", "select", "plan", "gate_up", "down", "combine"} <= general
+    m.moe_trace_enable(h.h, 0)
+    h.close()
+
+
+# -------------------------------------------------- GLM-5.2-shaped layers ----
+
+_GLM_CACHE: dict = {}
+
+
+def _glm(name):
+    if name not in _GLM_CACHE:
+        _GLM_CACHE.clear()
+        torch.cuda.empty_cache()
+        wl = CONFIGS[name]
+        _GLM_CACHE[name] = (wl, gen_layer(wl, device=DEV), HostExpertCache(wl))
+    return _GLM_CACHE[name]
+
+
+def test_glm_decode_tokens(m):
+    wl, L, cache = _glm("glm_decode")
+    h = m.MoELayer(L, 1)
+    for call in (0, 1, 2):
+        x = gen_activations(wl, 1, call=call)
+        _run_full(m, wl, L, x, cache=cache, handle=h)
+    h.close()
+
+
+def test_glm_verify_batch(m):
+    wl, L, cache = _glm("glm_verify")
+    x = gen_activations(wl, 4, call=0)
+    _run_full(m, wl, L, x, cache=cache)
+
+
+def test_glm_prefill_sampled(m):
+    wl, L, cache = _glm("glm_prefill")
+    x = gen_activations(wl, 512, call=0)
+    _, plan, _ = _run_full(m, wl, L, x, sample=[0, 1, 77, 255, 300, 511], cache=cache)
+    counts = plan.counts.cpu().numpy()
+    assert counts.max() >= 40 and (counts == 0).sum() >= 1  # uneven, Zipf-skewed load
+
+
+def test_glm_ragged_batch(m):
+    wl, L, cache = _glm("glm_prefill")
+    x = gen_activations(wl, 37, call=5)
+    _run_full(m, wl, L, x, sample=[0, 18, 36], cache=cache, max_tokens=64)
+
+
+def test_glm_stack_teacher_forced(m):
+    """24 resident layers, RMSNorm + residual, one token; layers checked
+    against the oracle on the GPU's own layer inputs."""
+    _GLM_CACHE.clear()
+    torch.cuda.empty_cache()
+    wl = CONFIGS["glm_stack"]
+    free, _ = torch.cuda.mem_get_info()
+    per = 5.6e9
+    n_layers = wl.layers if free > per * wl.layers + 20e9 else max(2, int((free - 20e9) // per))
+    layers = [gen_layer(wl, layer=i, device=DEV) for i in range(n_layers)]
+    handles = [m.MoELayer(L, 1) for L in layers]
+    gammas = [gen_norm_weight(wl, i).to(DEV) for i in range(n_layers)]
+    x = gen_activations(wl, 1, call=0, dtype="f32").to(DEV)
+    check = sorted({0, 1, n_layers // 2, n_layers - 1})
+    inputs = {}
+    for i in range(n_layers):
+        if i in check:
+            inputs[i] = x.clone()
+        handles[i].forward(x, y=x, gamma=gammas[i], eps=RMS_EPS, accumulate=True)
+    torch.cuda.synchronize()
+    final = x.cpu().numpy()
+    assert np.all(np.isfinite(final))
+    for i in check:
+        x_in = inputs[i].cpu().numpy()
+        g = gammas[i].cpu().numpy()
+        xd = inputs[i].clone()
+        plan = m.Plan(1, wl.shape.top_k, wl.shape.n_experts, DEV)
+        handles[i].forward(xd, y=xd, gamma=gammas[i], eps=RMS_EPS, accumulate=True, plan=plan)
+        torch.cuda.synchronize()
+        router = router_of(wl, i)
+        y_o, ids_o, w_o, _ = oracle_layer(wl, i, router, x_in, [0], eps=RMS_EPS, gamma=g,
+                                          resid=x_in)
+        assert np.array_equal(plan.topk_ids.cpu().numpy(), ids_o)
+        assert np.array_equal(plan.topk_w.cpu().numpy().view(np.uint32), w_o.view(np.uint32))
+        err = rel_err_per_token(xd.cpu().numpy() - x_in, y_o - x_in)
+        assert err.max() <= TOL, (i, err)
+    for h in handles:
+        h.close()

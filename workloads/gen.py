@@ -148,6 +148,12 @@ def gen_activations(w: Workload, T: int, call: int, layer: int = 0,
     return x.to(torch.float32).contiguous()
 
 
+def gen_norm_weight(w: Workload, layer: int) -> torch.Tensor:
+    """RMSNorm weight [H] fp32 ~U(0.5, 1.5) of one layer of a stacked workload."""
+    g = torch.Generator().manual_seed(w.seed * 65537 + layer * 257 + 3)
+    return (torch.rand(w.shape.hidden, generator=g) + 0.5).contiguous()
+
+
 @dataclass
 class LayerInputs:
     """All tensors of one MoE layer (device or host)."""
