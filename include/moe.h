@@ -74,7 +74,7 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
 /* Layer geometry.  Requirements (else MOE_ERR_UNSUPPORTED):
- *   hidden % 256 == 0 and 256 <= hidden <= 16384;
+ *   hidden % 256 == 0 and 256 <= hidden <= 12288;
  *   inter % 32 == 0, shared_inter % 32 == 0 (if n_shared), both <= 8192;
  *   1 <= n_experts <= 1024, n_experts % n_group == 0;
  *   1 <= topk_group <= n_group, 1 <= top_k <= 32,

@@ -28,8 +28,8 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 const char* check_config(const moe_config_t* c) {
   if (!c) return "cfg is NULL";
-  if (c->hidden % 256 != 0 || c->hidden < 256 || c->hidden > 16384)
-    return "hidden must be a multiple of 256 in [256, 16384]";
+  if (c->hidden % 256 != 0 || c->hidden < 256 || c->hidden > 12288)
+    return "hidden must be a multiple of 256 in [256, 12288]";
   if (c->inter % 32 != 0 || c->inter < 32 || c->inter > 8192)
     return "inter must be a multiple of 32 in [32, 8192]";
   if (c->n_shared != 0 && c->n_shared != 1) return "n_shared must be 0 or 1";

@@ -65,7 +65,7 @@ def test_workspace_bytes(m):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(hidden=300), dict(hidden=128), dict(inter=100), dict(n_experts=0),
+    dict(hidden=300), dict(hidden=128), dict(hidden=12544), dict(inter=100), dict(n_experts=0),
     dict(n_experts=2048), dict(n_group=3), dict(topk_group=5), dict(top_k=0),
     dict(top_k=33), dict(top_k=9, topk_group=2), dict(group_size=64), dict(max_tokens=0),
     dict(n_shared=2), dict(shared_inter=100), dict(routed_scaling_factor=float("nan")),
