@@ -23,6 +23,21 @@ def rel_err_per_token(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.abs(y - ref).max(axis=1) / den
 
 
+def resid_err_per_token(y: np.ndarray, y_ref: np.ndarray, resid: np.ndarray) -> np.ndarray:
+    """Error of a residual-form output y = resid + MoE(...).
+
+    Both sides round resid + v once in fp32, so a difference d in v can
+    move y by d plus one unit in the last place of y: that ulp is allowed on
+    top, and the rest is measured against the MoE output y_ref - resid."""
+    y = np.asarray(y, np.float64).reshape(y_ref.shape[0], -1)
+    ref = np.asarray(y_ref, np.float64).reshape(y_ref.shape[0], -1)
+    delta = ref - np.asarray(resid, np.float64).reshape(ref.shape)
+    ulp = np.spacing(np.abs(np.asarray(y_ref, np.float32))).astype(np.float64).reshape(ref.shape)
+    excess = np.maximum(np.abs(y - ref) - ulp, 0.0)
+    den = np.maximum(np.abs(delta).max(axis=1), 1e-30)
+    return excess.max(axis=1) / den
+
+
 def router_of(workload, layer: int = 0):
     seed = workload.seed + layer if workload.layers > 1 else workload.seed
     rw, rb = gen_router(workload.shape, seed, layer, workload.bias_kind, workload.zipf_s)

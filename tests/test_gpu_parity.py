@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import oracle
-from parity_util import RMS_EPS, TOL, oracle_layer, rel_err_per_token, router_of
+from parity_util import (RMS_EPS, TOL, oracle_layer, rel_err_per_token, resid_err_per_token,
+                         router_of)
 from workloads import CONFIGS
 from workloads.configs import LayerShape, Workload
 from workloads.gen import HostExpertCache, gen_activations, gen_layer, gen_norm_weight
@@ -214,7 +215,7 @@ def test_residual_in_place(m):
             torch.cuda.synchronize()
             y_o, _, _, _ = oracle_layer(wl, 0, router_of(wl), x0.numpy(), range(T), eps=RMS_EPS,
                                         gamma=gamma.numpy(), resid=x0.numpy())
-            err = rel_err_per_token(xd.cpu().numpy() - x0.numpy(), y_o - x0.numpy())
+            err = resid_err_per_token(xd.cpu().numpy(), y_o, x0.numpy())
             assert err.max() <= TOL
         h.close()
 
@@ -314,7 +315,7 @@ def test_glm_stack_teacher_forced(m):
                                           resid=x_in)
         assert np.array_equal(plan.topk_ids.cpu().numpy(), ids_o)
         assert np.array_equal(plan.topk_w.cpu().numpy().view(np.uint32), w_o.view(np.uint32))
-        err = rel_err_per_token(xd.cpu().numpy() - x_in, y_o - x_in)
+        err = resid_err_per_token(xd.cpu().numpy(), y_o, x_in)
         assert err.max() <= TOL, (i, err)
     for h in handles:
         h.close()
