@@ -44,7 +44,8 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons; only the samples
+    taken between mark_start() and mark_stop() are summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -55,6 +56,7 @@ class ClockSampler:
         self.samples = []
         self.proc = None
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -72,7 +74,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 7:
-                self.samples.append(parts)
+                self.samples.append((time.monotonic(), parts))
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_stop(self):
+        self.t1 = time.monotonic()
+
+    def wait_first(self, timeout=10.0):
+        end = time.monotonic() + timeout
+        while not self.samples and time.monotonic() < end and self.proc is not None:
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is not None:
@@ -89,7 +102,9 @@ class ClockSampler:
         mx = None
         reasons = set()
         names = ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
-        for p in self.samples:
+        inside = [p for t, p in self.samples
+                  if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        for p in inside:
             try:
                 sm.append(float(p[0]))
                 mx = float(p[1])
@@ -169,6 +184,10 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
 
 # ------------------------------------------------------------- workloads ----
 
+def workload_key(wl, experts=None):
+    return f"{wl.name}_E{experts}" if experts else wl.name
+
+
 def make_workload(name, experts=None, calls=None):
     from workloads import CONFIGS
     from workloads.configs import LayerShape, Workload
@@ -231,13 +250,14 @@ class GpuRun:
                 h.forward(y, y=y, gamma=g, eps=self.wl.rmsnorm_eps, accumulate=True,
                           stream=self.stream)
 
-    def timed_pass(self, e2e=False):
+    def timed_pass(self, e2e=False, flush=True):
         """Device ms of one step: sum over calls of the forward's events."""
         import torch
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(self.calls)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(self.calls)]
         for c in range(self.calls):
-            self.flush()
+            if flush:
+                self.flush()
             starts[c].record()
             if e2e:
                 self.x[c].copy_(self.x_host[c], non_blocking=True)
@@ -386,7 +406,7 @@ def run_reference(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="glm_decode",
@@ -416,24 +436,30 @@ def main():
 
     run = GpuRun(wl, dev, args.layers)
     sh = wl.shape
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(max(args.warmup, 3)):
         run.timed_pass()
     run.check_status()
+    clocks.wait_first()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier()
+    clocks.mark_start()
     dev_ms = 0.0
     for _ in range(args.steps):
         dev_ms += run.timed_pass()
     barrier()
+    clocks.mark_stop()
     clocks.stop()
     run.check_status()
+
+    # steady state without the L2 flush (weights of popular experts may stay in L2)
+    unflushed_ms = run.timed_pass(flush=False)
 
     # end to end: inputs copied from pinned host memory and outputs read back
     # inside each forward's events
@@ -494,12 +520,13 @@ def main():
                 "tokens_per_step": tokens_step, "x_dtype": "f32" if run.norm else wl.x_dtype,
                 "weights": "int4 offset-binary, group 32, fp16 scales",
                 "l2": "flushed (512 MiB read) before every forward, outside the events",
+                "unflushed_tokens_per_s": round(tokens_step / (unflushed_ms / 1000.0), 1),
                 "parallelism": f"replicas x{world}",
             },
             "roofline": {"bound": "hbm", "kernel": dominant,
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "traffic": ncu_traffic(dominant, wl.name),
+                         "traffic": ncu_traffic(dominant, workload_key(wl, args.experts)),
                          "algorithmic_bytes_per_launch": kb,
                          "avg_launch_us": round(1000 * per_launch_ms, 3),
                          "duration_source": "CUDA events between the kernels in a traced pass "
