@@ -199,6 +199,42 @@ const char* moe_trace_phase_name(int phase);
  * kernel returned early; the outputs of that call are not valid. */
 moe_status_t moe_device_status(moe_layer_t* h, int32_t* flags);
 
+/* Routing without any allocation (the pages have no counterpart: it serves
+ * this library's callers, not a step of the method).
+ *
+ * Same result as moe_route on a handle created with cfg: optional RMSNorm,
+ * router logits, noaux_tc selection and the routing plan of T tokens, written
+ * to the non-NULL members of *plan_out.  It takes the router weight and bias
+ * directly instead of a handle, and keeps its intermediate buffers in one
+ * fixed 2 MiB block of static device memory per device instead of a
+ * workspace.  It is meant for callers that cannot allocate device memory at
+ * run time: a serving process that hands all of HBM to its expert cache at
+ * start-up and allows no later cudaMalloc, or a router-only prefetcher that
+ * decides which experts to fetch next without holding their weights (and so
+ * without a layer handle).  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ *   cfg       geometry; validated like moe_layer_create (MOE_ERR_UNSUPPORTED),
+ *             max_tokens is not used
+ *   router_w  [E][H] fp32, router_bias [E] fp32, x [T][H] of dtype,
+ *             rms_gamma [H] or NULL: device pointers, 16-byte aligned
+ *   plan_out  as for moe_route (NULL members are kept in the scratch)
+ * Limit: T * (hidden + n_experts) * 4 + 16 * T * top_k + 12 * n_experts, each
+ * buffer rounded up to 256 bytes, must fit in the 2 MiB block (for example
+ * T <= 64 at hidden = 6144, n_experts = 256, top_k = 8); larger T returns
+ * MOE_ERR_CAPACITY with the sizes in moe_last_error(NULL).  T == 0 is a no-op.
+ * The first call on a device looks up that device's block
+ * (cudaGetSymbolAddress) with the device current; make that first call before
+ * capturing any stream.  Nothing in the block needs to start at zero.  All
+ * calls on one device share the block: two calls in flight at the same time
+ * (on different streams or from different threads) race and give wrong
+ * results, so serialise them.  Errors are reported through
+ * moe_last_error(NULL) of the calling thread. */
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* router_w,
+                               const float* router_bias, const void* x, moe_dtype_t dtype,
+                               int T, const float* rms_gamma, float rms_eps,
+                               moe_plan_t* plan_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -270,6 +270,16 @@ void free_trace(moe_layer* h) {
 
 }  // namespace
 
+namespace moe {
+// Message for moe_last_error(NULL) on this thread (entry points without a handle).
+void set_thread_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_config_t* cfg) {

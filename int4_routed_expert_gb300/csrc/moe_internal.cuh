@@ -64,6 +64,9 @@ struct moe_layer {
 
 namespace moe {
 
+// Sets the message moe_last_error(NULL) returns on this thread.
+void set_thread_error(const char* fmt, ...);
+
 // ---- launchers (each returns the cudaError_t of its launch) --------------
 
 // x (fp32 or bf16) -> xf fp32, optionally RMSNorm'd with gamma (fp64 sum of

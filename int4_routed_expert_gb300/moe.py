@@ -59,7 +59,7 @@ class moe_plan_t(C.Structure):
 
 EXPORTED = ("moe_layer_create", "moe_route", "moe_forward", "moe_destroy",
             "moe_last_error", "moe_workspace_bytes", "moe_trace_enable", "moe_trace_read",
-            "moe_trace_phase_name", "moe_device_status")
+            "moe_trace_phase_name", "moe_device_status", "moe_route_noalloc")
 
 _lib = None
 
@@ -98,6 +98,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.moe_trace_phase_name.argtypes = [C.c_int]
     L.moe_device_status.restype = C.c_int
     L.moe_device_status.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
+    L.moe_route_noalloc.restype = C.c_int
+    L.moe_route_noalloc.argtypes = [C.POINTER(moe_config_t), C.c_void_p, C.c_void_p, C.c_void_p,
+                                    C.c_int, C.c_int, C.c_void_p, C.c_float,
+                                    C.POINTER(moe_plan_t), C.c_void_p]
     _lib = L
     return L
 
@@ -131,6 +135,14 @@ def moe_forward(h, x: int, dtype: int, T: int, y: int, gamma: int | None, eps: f
                 accumulate: int, plan: moe_plan_t | None, stream: int | None) -> None:
     _check(load().moe_forward(h, x, dtype, T, y, gamma, eps, accumulate,
                               C.byref(plan) if plan is not None else None, stream), h)
+
+
+def moe_route_noalloc(cfg: moe_config_t, router_w: int, router_bias: int, x: int, dtype: int,
+                      T: int, gamma: int | None, eps: float, plan: moe_plan_t | None,
+                      stream: int | None) -> None:
+    """Routing of T tokens without a handle and without any allocation."""
+    _check(load().moe_route_noalloc(C.byref(cfg), router_w, router_bias, x, dtype, T, gamma, eps,
+                                    C.byref(plan) if plan is not None else None, stream), None)
 
 
 def moe_destroy(h) -> None:
