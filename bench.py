@@ -169,6 +169,10 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
     ns = 1 if sh.n_shared else 0
     router = E * H * 4 + E * 4
     hrows = (T * k + T * ns) * sh.inter * 4
+    if phase == "decode_fused":
+        return (router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh)
+                + n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
+                + 2 * hrows + T * H * 4)
     if phase == "decode_router_gate_up":
         return router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh) + hrows
     if phase == "decode_down_combine":

@@ -251,7 +251,7 @@ cudaError_t run_route(moe_layer* h, const void* x, moe_dtype_t dt, int T, const 
 
 const char* kPhaseNames[MOE_N_PHASES] = {
     "prep",   "router_logits", "select",  "plan",
-    "gate_up", "down",         "combine", "unused",
+    "gate_up", "down",         "combine", "decode_fused",
     "decode_router_gate_up", "decode_down_combine"};
 
 void free_trace(moe_layer* h) {

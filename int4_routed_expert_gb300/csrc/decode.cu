@@ -1,6 +1,6 @@
 // Host side of the fused small-batch path: eligibility, sizes and the
 // two-kernel launch chain (see decode_common.cuh).
-#include "decode_common.cuh"
+#include "decode_fused.cuh"
 
 namespace moe {
 namespace dec {
@@ -11,6 +11,12 @@ cudaError_t launch_dec_c_nt1(const DecArgs& a, int cpl, bool h_smem, size_t smem
                              bool pdl, cudaStream_t s);
 cudaError_t launch_dec_c_nt4(const DecArgs& a, int cpl, size_t smem, int n_sm, bool pdl,
                              cudaStream_t s);
+// fused single-token kernel; returns cudaErrorInvalidValue for an
+// uninstantiated (H, I) chunk combination
+cudaError_t launch_dec_fused_i1(const DecArgs& a, int cpl_h, size_t smem, int n_sm,
+                                cudaStream_t s);
+cudaError_t launch_dec_fused_i2(const DecArgs& a, int cpl_h, size_t smem, int n_sm,
+                                cudaStream_t s);
 
 namespace {
 
@@ -34,6 +40,15 @@ Sizes sizes_for(const Shape& sh, int T, int n_sm) {
              c_smem_bytes(sh, T, z.NT, true, hstride) <= kHSmemBudget;
   z.c = c_smem_bytes(sh, T, z.NT, z.h_smem, hstride);
   return z;
+}
+
+// The fused kernel serves T == 1 when its shared memory fits and the
+// intermediate size is one of its instantiations (h kept in registers).
+bool fused_ok(const Shape& sh, int T, int n_sm) {
+  if (T != 1) return false;
+  const int ci = chunks_per_lane(sh.I);
+  if (ci != 1 && ci != 2) return false;
+  return fused_smem_bytes(sh, n_sm) <= kSmemLimit;
 }
 
 }  // namespace
@@ -69,9 +84,20 @@ cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const 
   a.ws = ws;
   a.y = y;
   a.accumulate = accumulate;
-  // every CTA of dec_ab adds one to the grid-barrier counter per call
+  // every CTA adds one to the grid-barrier counter per barrier round;
+  // *calls counts the rounds of this handle so far
   a.gtarget = (*calls + 1) * static_cast<unsigned long long>(n_sm);
+  a.gtarget2 = (*calls + 2) * static_cast<unsigned long long>(n_sm);
   const int cpl_h = chunks_per_lane(sh.H), cpl_i = chunks_per_lane(sh.I);
+  if (fused_ok(sh, T, n_sm)) {
+    const size_t smem = fused_smem_bytes(sh, n_sm);
+    cudaError_t e = cpl_i == 1 ? launch_dec_fused_i1(a, cpl_h, smem, n_sm, s)
+                               : launch_dec_fused_i2(a, cpl_h, smem, n_sm, s);
+    if (e != cudaSuccess) return e;
+    *calls += 2;
+    pm.mark(7);
+    return cudaSuccess;
+  }
   cudaError_t e = z.NT == 1 ? launch_dec_ab_nt1(a, cpl_h, z.ab, n_sm, s)
                             : launch_dec_ab_nt4(a, cpl_h, z.ab, n_sm, s);
   if (e != cudaSuccess) return e;

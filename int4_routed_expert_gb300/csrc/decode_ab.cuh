@@ -23,38 +23,6 @@
 namespace moe {
 namespace dec {
 
-__device__ __forceinline__ void gbar_arrive(unsigned long long* p) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long gbar_load(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Lane 0 polls the grid-barrier counter (bounded); returns false on timeout.
-__device__ inline bool gbar_wait(unsigned long long* p, unsigned long long target, int* err) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
-    if (gbar_load(p) < target) {
-      const long long t0 = clock64();
-      while (gbar_load(p) < target) {
-        if (clock64() - t0 > kWaitClocks) {
-          atomicOr(err, kErrWaitTimeout);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  __threadfence();
-  return ok != 0;
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int wi) {
   return wi == 0 ? q.x : wi == 1 ? q.y : wi == 2 ? q.z : q.w;
 }
@@ -161,67 +129,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) dec_ab_kernel(const __grid_cons
   refill();
 
   // 3. router logits of this CTA's experts
-  if (warp < kRouterWarps) {
-    const int Lseg = H / kSeg, chunks = Lseg / 4;
-    float acc[kMaxLocalExperts][NT];
-#pragma unroll
-    for (int l = 0; l < kMaxLocalExperts; ++l)
-#pragma unroll
-      for (int t = 0; t < NT; ++t) acc[l][t] = 0.0f;
-    for (int c = lane; c < chunks; c += 32) {
-      const int kk = warp * Lseg + 4 * c;
-      float4 xv[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        xv[t] = t < T ? xhat4(a, static_cast<size_t>(t) * H + kk, kk,
-                              a.gamma != nullptr ? rfs[t] : 1.0f)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int l = 0; l < kMaxLocalExperts; ++l) {
-        const int e = blockIdx.x + l * gridDim.x;
-        if (l < L && e < E) {
-          const float4 w4 =
-              __ldg(reinterpret_cast<const float4*>(a.w.router_w + static_cast<size_t>(e) * H + kk));
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            float s = acc[l][t];
-            s = __fmaf_rn(xv[t].x, w4.x, s);
-            s = __fmaf_rn(xv[t].y, w4.y, s);
-            s = __fmaf_rn(xv[t].z, w4.z, s);
-            s = __fmaf_rn(xv[t].w, w4.w, s);
-            acc[l][t] = s;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int l = 0; l < kMaxLocalExperts; ++l) {
-      if (l >= L) break;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float p = segment_tree(acc[l][t]);
-        if (lane == 0) lseg[(l * kRouterWarps + warp) * NT + t] = p;
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kRouterWarps * 32) : "memory");
-    if (warp == 0) {
-      const int l = lane / NT, t = lane % NT;
-      const int e = blockIdx.x + l * gridDim.x;
-      if (l < L && t < T && e < E) {
-        float sg[kSeg];
-#pragma unroll
-        for (int s = 0; s < kSeg; ++s) sg[s] = lseg[(l * kRouterWarps + s) * NT + t];
-        const float logit = segments_sum(sg);
-        const float sv = router_sigmoid(logit);
-        const size_t o = static_cast<size_t>(t) * E + e;
-        ws.logits[o] = logit;
-        ws.sval[o] = sv;
-        ws.skey[o] = __fadd_rn(sv, __ldg(a.w.router_bias + e));
-      }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) gbar_arrive(ws.gbar);
-    }
+  router_cta<NT, CPL>(a, lseg, rfs);
+  if (warp == 0) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) gbar_arrive(ws.gbar);
   }
   pdl_launch_dependents();
 

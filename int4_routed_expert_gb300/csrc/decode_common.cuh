@@ -41,7 +41,8 @@ struct DecArgs {
   Workspace ws;
   float* y;
   int accumulate;
-  unsigned long long gtarget;  // grid-barrier count that completes this call's barrier
+  unsigned long long gtarget;   // grid-barrier count that completes this call's first barrier
+  unsigned long long gtarget2;  // ... and its second (fused single-token kernel)
 };
 
 // Balanced split of n items over B parts: [begin, end) of part b.
@@ -116,6 +117,42 @@ __device__ __forceinline__ void swz_store4(float* dst, int k, float4 v) {
   *reinterpret_cast<float4*>(dst + swz_index(g, i)) = v;
 }
 
+// ---- grid barrier: a monotonic 64-bit counter in the workspace ---------
+//
+// Every CTA adds one per barrier round; round r of the handle completes when
+// the counter reaches r * gridDim.x.  Waits are bounded.
+__device__ __forceinline__ void gbar_arrive(unsigned long long* p) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long gbar_load(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Lane 0 polls the grid-barrier counter (bounded); returns false on timeout.
+__device__ inline bool gbar_wait(unsigned long long* p, unsigned long long target, int* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    if (gbar_load(p) < target) {
+      const long long t0 = clock64();
+      while (gbar_load(p) < target) {
+        if (clock64() - t0 > kWaitClocks) {
+          atomicOr(err, kErrWaitTimeout);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  __threadfence();
+  return ok != 0;
+}
+
 // The routing plan of the call, one selected expert ("slot") per lane.
 struct LanePlan {
   int n_act;       // slots (distinct experts), warp-uniform
@@ -123,6 +160,7 @@ struct LanePlan {
   int p0;          // first plan position of the slot
   int n;           // entries of the slot
   unsigned tmask;  // tokens of the slot (bit t)
+  float w;         // gate weight of the slot's first entry
 };
 
 template <int EPL>
@@ -135,8 +173,8 @@ __device__ __forceinline__ void select_token(const DecArgs& a, int t, int& id, f
 // published scores (bit-identical in every warp), then the plan: entries
 // i = t*k + j grouped by expert ascending, ascending i inside an expert.
 // With `publish`, the plan is also written to the workspace.
-static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, bool publish,
-                                             LanePlan& lp) {
+__device__ __forceinline__ void warp_route_plan_inl(const DecArgs& a, int epl, bool publish,
+                                                   LanePlan& lp) {
   const int lane = threadIdx.x & 31;
   const int k = a.sh.k, T = a.T, N = T * k;
   int my_id = 0;
@@ -182,6 +220,7 @@ static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, b
   lp.p0 = 0;
   lp.n = 0;
   lp.tmask = 0;
+  lp.w = 0.0f;
   for (unsigned m = leaders; m; m &= m - 1) {
     const int l = __ffs(m) - 1;
     const int al = __shfl_sync(0xffffffffu, before, l);
@@ -189,11 +228,13 @@ static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, b
     const int bl = __shfl_sync(0xffffffffu, base, l);
     const int cl = __shfl_sync(0xffffffffu, cnt, l);
     const unsigned tl = __shfl_sync(0xffffffffu, tmask, l);
+    const float wl = __shfl_sync(0xffffffffu, my_w, l);
     if (lane == al) {
       lp.e = el;
       lp.p0 = bl;
       lp.n = cl;
       lp.tmask = tl;
+      lp.w = wl;
     }
   }
   if (publish) {
@@ -212,6 +253,146 @@ static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, b
       ws.dslot[64 + lane] = lp.n;
     }
     if (lane == 0) *ws.n_active = lp.n_act;
+    // per-expert counts and exclusive offsets over all E experts
+    for (int e0 = 0; e0 < a.sh.E; e0 += 32) {
+      const int ex = e0 + lane;
+      int c = 0, off = 0;
+      for (int q = 0; q < lp.n_act; ++q) {
+        const int eq = __shfl_sync(0xffffffffu, lp.e, q);
+        const int nq = __shfl_sync(0xffffffffu, lp.n, q);
+        if (eq == ex) c = nq;
+        if (eq < ex) off += nq;
+      }
+      if (ex < a.sh.E) {
+        ws.counts[ex] = c;
+        ws.offsets[ex] = off;
+      }
+    }
+    if (lane == 0) ws.offsets[a.sh.E] = N;
+  }
+}
+
+// Router logits from shared memory: xn = x_hat in natural order [H], wr =
+// the CTA's router rows [L][H] (expert blockIdx.x + l * gridDim.x).  Same
+// fixed order and roundings as router_cta; warp 0 writes the results.
+__device__ __forceinline__ void router_cta_smem(const DecArgs& a, const float* xn, const float* wr,
+                                                float* lseg) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kRouterWarps) return;
+  const int H = a.sh.H, E = a.sh.E;
+  const int L = (E + gridDim.x - 1) / gridDim.x;
+  const int Lseg = H / kSeg, chunks = Lseg / 4;
+  for (int l = 0; l < L; ++l) {
+    const int e = blockIdx.x + l * gridDim.x;
+    if (e >= E) break;
+    const float* w = wr + static_cast<size_t>(l) * H;
+    float acc = 0.0f;
+    for (int c = lane; c < chunks; c += 32) {
+      const int kk = warp * Lseg + 4 * c;
+      const float4 xv = *reinterpret_cast<const float4*>(xn + kk);
+      const float4 w4 = *reinterpret_cast<const float4*>(w + kk);
+      acc = __fmaf_rn(xv.x, w4.x, acc);
+      acc = __fmaf_rn(xv.y, w4.y, acc);
+      acc = __fmaf_rn(xv.z, w4.z, acc);
+      acc = __fmaf_rn(xv.w, w4.w, acc);
+    }
+    const float p = segment_tree(acc);
+    if (lane == 0) lseg[l * kRouterWarps + warp] = p;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kRouterWarps * 32) : "memory");
+  if (warp == 0) {
+    const int e = blockIdx.x + lane * gridDim.x;
+    if (lane < L && e < E) {
+      float sg[kSeg];
+#pragma unroll
+      for (int s = 0; s < kSeg; ++s) sg[s] = lseg[lane * kRouterWarps + s];
+      const float logit = segments_sum(sg);
+      const float sv = router_sigmoid(logit);
+      a.ws.logits[e] = logit;
+      a.ws.sval[e] = sv;
+      a.ws.skey[e] = __fadd_rn(sv, __ldg(a.w.router_bias + e));
+    }
+  }
+}
+
+// Out-of-line copy for kernels with many instantiations.
+static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, bool publish,
+                                                    LanePlan& lp) {
+  warp_route_plan_inl(a, epl, publish, lp);
+}
+
+// Router logits of this CTA's experts (blockIdx.x + l * gridDim.x) by warps
+// 0..7, one logit segment each, in the fixed order; warp 0 then writes the
+// logits, scores and keys of those experts.  Called by every warp; only
+// warps 0..7 take part (they meet on named barrier 1).  rfs: the tokens'
+// RMSNorm scales (read when gamma is given).  The caller publishes.
+// RC: upper bound of the chunks a lane handles (H / 1024, at least 1); the
+// loop is unrolled so that all of a lane's loads are in flight together.
+template <int NT, int RC>
+__device__ __forceinline__ void router_cta(const DecArgs& a, float* lseg, const float* rfs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kRouterWarps) return;
+  const int H = a.sh.H, E = a.sh.E, T = a.T;
+  const int L = (E + gridDim.x - 1) / gridDim.x;
+  const int Lseg = H / kSeg, chunks = Lseg / 4;
+  float acc[kMaxLocalExperts][NT];
+#pragma unroll
+  for (int l = 0; l < kMaxLocalExperts; ++l)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[l][t] = 0.0f;
+#pragma unroll
+  for (int ci = 0; ci < RC; ++ci) {
+    const int c = lane + 32 * ci;
+    if (c >= chunks) break;
+    const int kk = warp * Lseg + 4 * c;
+    float4 xv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      xv[t] = t < T ? xhat4(a, static_cast<size_t>(t) * H + kk, kk,
+                            a.gamma != nullptr ? rfs[t] : 1.0f)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int l = 0; l < kMaxLocalExperts; ++l) {
+      const int e = blockIdx.x + l * gridDim.x;
+      if (l < L && e < E) {
+        const float4 w4 =
+            __ldg(reinterpret_cast<const float4*>(a.w.router_w + static_cast<size_t>(e) * H + kk));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          float s = acc[l][t];
+          s = __fmaf_rn(xv[t].x, w4.x, s);
+          s = __fmaf_rn(xv[t].y, w4.y, s);
+          s = __fmaf_rn(xv[t].z, w4.z, s);
+          s = __fmaf_rn(xv[t].w, w4.w, s);
+          acc[l][t] = s;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int l = 0; l < kMaxLocalExperts; ++l) {
+    if (l >= L) break;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float p = segment_tree(acc[l][t]);
+      if (lane == 0) lseg[(l * kRouterWarps + warp) * NT + t] = p;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kRouterWarps * 32) : "memory");
+  if (warp == 0) {
+    const int l = lane / NT, t = lane % NT;
+    const int e = blockIdx.x + l * gridDim.x;
+    if (l < L && t < T && e < E) {
+      float sg[kSeg];
+#pragma unroll
+      for (int s = 0; s < kSeg; ++s) sg[s] = lseg[(l * kRouterWarps + s) * NT + t];
+      const float logit = segments_sum(sg);
+      const float sv = router_sigmoid(logit);
+      const size_t o = static_cast<size_t>(t) * E + e;
+      a.ws.logits[o] = logit;
+      a.ws.sval[o] = sv;
+      a.ws.skey[o] = __fadd_rn(sv, __ldg(a.w.router_bias + e));
+    }
   }
 }
 

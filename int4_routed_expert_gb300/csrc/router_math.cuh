@@ -200,10 +200,22 @@ __host__ __device__ inline int fast_select_epl(const Shape& sh) {
   return epl;
 }
 
+// Order-preserving code of a float key: a > b  <=>  code(a) > code(b) for
+// non-NaN keys other than -0 (a key s + b with s > 0 is never -0).  Code 0
+// is left for "no candidate".
+__device__ __forceinline__ uint32_t key_code(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Register-resident selection of one token by one warp (shapes accepted by
 // fast_select_epl).  gkey / gs: the token's [E] keys and scores in global
-// memory (read through L2).  Same result as warp_select.  Lanes < k receive
-// (id, w) of slot `lane` in out_id / out_w; returns k.
+// memory (read through L2).  Same result as warp_select: groups are ranked
+// in one step (each group leader counts the groups that rank before it);
+// each of the k rounds takes the maximum key code over the warp with one
+// redux.sync, and the lowest lane holding it wins, which is the lower
+// expert id on a tie because lane L holds experts L*EPL .. L*EPL+EPL-1.
+// Lanes < k receive (id, w) of slot `lane` in out_id / out_w.
 template <int EPL>
 __device__ __forceinline__ void warp_select_regs(const float* gkey, const float* gs,
                                                  const Shape& sh, int& out_id, float& out_w) {
@@ -247,41 +259,42 @@ __device__ __forceinline__ void warp_select_regs(const float* gkey, const float*
   }
   const float gscore = (G >= 2) ? __fadd_rn(a, b) : a;
   const int my_group = lane / lpg;
-  // keep topk_group groups
-  uint32_t kept = 0;
-  for (int r = 0; r < sh.topk_group; ++r) {
-    float bv = gscore;
-    int bi = (lane % lpg == 0 && !((kept >> my_group) & 1u)) ? my_group : kNoIndex;
-    warp_argmax(bv, bi);
-    kept |= 1u << bi;
+  // a group is kept when fewer than topk_group groups rank before it
+  int before = 0;
+  for (int g2 = 0; g2 < sh.n_group; ++g2) {
+    const float o = __shfl_sync(0xffffffffu, gscore, g2 * lpg);
+    before += (o > gscore || (o == gscore && g2 < my_group)) ? 1 : 0;
   }
-  const bool in_kept = (kept >> my_group) & 1u;
-  uint32_t taken = 0;
+  const bool in_kept = before < sh.topk_group;
+  // candidate codes (0 = not a candidate)
+  uint32_t code[EPL];
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) code[q] = in_kept ? key_code(kv[q]) : 0u;
   float my_s = 0.0f, sum = 0.0f;
   int my_id = 0;
   for (int j = 0; j < sh.k; ++j) {
-    float bv = 0.0f;
-    int bi = kNoIndex;
-    if (in_kept) {
+    uint32_t best = 0;
 #pragma unroll
-      for (int q = 0; q < EPL; ++q) {
-        if ((taken >> q) & 1u) continue;
-        if (bi == kNoIndex || kv[q] > bv) {  // ascending ids: strict > keeps the lower id
-          bv = kv[q];
-          bi = lane * EPL + q;
-        }
-      }
-    }
-    warp_argmax(bv, bi);
-    const int owner = bi / EPL, slot = bi % EPL;
+    for (int q = 0; q < EPL; ++q) best = max(best, code[q]);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+    const unsigned holders = __ballot_sync(0xffffffffu, best == m && m != 0u);
+    const int owner = __ffs(holders) - 1;
+    // the owner's lowest slot holding the maximum
+    int slot = EPL;
+#pragma unroll
+    for (int q = EPL - 1; q >= 0; --q) slot = (code[q] == m) ? q : slot;
     float sl = 0.0f;
 #pragma unroll
     for (int q = 0; q < EPL; ++q) sl = (q == slot) ? sv[q] : sl;
     const float sj = __shfl_sync(0xffffffffu, sl, owner);
-    if (lane == owner) taken |= 1u << slot;
+    const int oslot = __shfl_sync(0xffffffffu, slot, owner);
+    if (lane == owner) {
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) code[q] = (q == slot) ? 0u : code[q];
+    }
     if (lane == j) {
       my_s = sj;
-      my_id = bi;
+      my_id = owner * EPL + oslot;
     }
     sum = __fadd_rn(sum, sj);
   }

@@ -228,12 +228,15 @@ def test_trace_phases(m):
     m.moe_trace_enable(h.h, 3)
     h.forward(gen_activations(wl, 1, call=0).to(DEV))
     h.forward(gen_activations(wl, 20, call=1).to(DEV))
+    h.forward(gen_activations(wl, 3, call=2).to(DEV))
     names, rows = m.moe_trace_read(h.h, 3)
-    assert len(rows) == 2 and len(names) == 10
+    assert len(rows) == 3 and len(names) == 10
     small = {n for n, v in zip(names, rows[0]) if v > 0}
     general = {n for n, v in zip(names, rows[1]) if v > 0}
-    assert small == {"decode_router_gate_up", "decode_down_combine"}
+    assert small == {"decode_fused"}
     assert {"prep", "router_logits", "select", "plan", "gate_up", "down", "combine"} <= general
+    batch = {n for n, v in zip(names, rows[2]) if v > 0}
+    assert batch == {"decode_router_gate_up", "decode_down_combine"}
     m.moe_trace_enable(h.h, 0)
     h.close()
 
