@@ -183,6 +183,15 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
     if phase == "down":
         return (n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
                 + hrows + (T * k + T * ns) * H * 4)
+    rows = T * k + T * ns  # plan rows + shared-expert rows of the f16 buffers
+    if phase == "tc_prep":
+        return T * H * 4 + rows * H * 2
+    if phase == "tc_gate_up":
+        return (n_act * expert_gate_up_bytes(sh) + ns * expert_gate_up_bytes(sh)
+                + rows * H * 2 + rows * sh.inter * 2)
+    if phase == "tc_down":
+        return (n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
+                + rows * sh.inter * 2 + rows * H * 4)
     return None
 
 

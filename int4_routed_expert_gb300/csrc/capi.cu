@@ -72,7 +72,7 @@ const char* check_weights(const moe_config_t* c, const moe_weights_t* w) {
 
 // Workspace layout: each buffer 256-byte aligned, in this order.
 struct Layout {
-  size_t off[17];
+  size_t off[21];
   size_t total;
   int hstride;
 };
@@ -89,7 +89,10 @@ Layout layout_for(const moe_config_t* c) {
   L.hstride = ((Imax / 32 + 31) / 32) * 1024;
   const size_t N = Tm * k, R = N + Tm;
   const size_t Ts = Tm < 4 ? Tm : 4;
-  const size_t sz[17] = {
+  // f16 rows and chunk list of the tensor-core path (shapes it takes only)
+  const bool tc = c->hidden % 256 == 0 && c->inter % 256 == 0 &&
+                  (!c->n_shared || c->shared_inter % 256 == 0);
+  const size_t sz[21] = {
       Tm * H * 4,            // xf
       Tm * E * 4,            // logits
       N * 4,                 // ids
@@ -107,9 +110,13 @@ Layout layout_for(const moe_config_t* c) {
       256,                   // dev_err
       3 * 32 * 4,            // dslot
       256,                   // gbar
+      tc ? R * H * 2 : 0,    // x16
+      tc ? R * Imax * 2 : 0, // h16
+      tc ? moe::tc_max_chunks(c->max_tokens, c->top_k, c->n_experts) * 16 : 0,  // chunks
+      4,                     // n_rchunks
   };
   size_t o = 0;
-  for (int i = 0; i < 17; ++i) {
+  for (int i = 0; i < 21; ++i) {
     L.off[i] = o;
     o += up256(sz[i]);
   }
@@ -136,6 +143,10 @@ Workspace carve(char* base, const Layout& L) {
   w.dev_err = reinterpret_cast<int32_t*>(base + L.off[14]);
   w.dslot = reinterpret_cast<int32_t*>(base + L.off[15]);
   w.gbar = reinterpret_cast<unsigned long long*>(base + L.off[16]);
+  w.x16 = reinterpret_cast<__half*>(base + L.off[17]);
+  w.h16 = reinterpret_cast<__half*>(base + L.off[18]);
+  w.chunks = reinterpret_cast<int4*>(base + L.off[19]);
+  w.n_rchunks = reinterpret_cast<int32_t*>(base + L.off[20]);
   w.hstride = L.hstride;
   return w;
 }
@@ -250,9 +261,10 @@ cudaError_t run_route(moe_layer* h, const void* x, moe_dtype_t dt, int T, const 
 }
 
 const char* kPhaseNames[MOE_N_PHASES] = {
-    "prep",   "router_logits", "select",  "plan",
-    "gate_up", "down",         "combine", "decode_fused",
-    "decode_router_gate_up", "decode_down_combine"};
+    "prep",       "router_logits", "select",  "plan",
+    "gate_up",    "down",          "combine", "decode_fused",
+    "decode_router_gate_up", "decode_down_combine",
+    "tc_prep",    "tc_gate_up",    "tc_down"};
 
 void free_trace(moe_layer* h) {
   if (h->trace_ev) {
@@ -339,6 +351,9 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
     delete h;
     return MOE_ERR_CUDA;
   }
+  // tensor-core path: TMA tensor maps over the weights and the f16 rows
+  h->tc = moe::tc_path_ok(h->sh) ? moe::tc_create_maps(h->w, h->sh, h->ws, cfg->max_tokens)
+                                 : nullptr;
   *out = h;
   return MOE_OK;
 }
@@ -400,6 +415,25 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
     e = moe::launch_decode(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
                            h->n_sm, &h->decode_calls, pm, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (small-batch path)");
+  } else if (h->tc) {
+    e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
+    if (e == cudaSuccess) {
+      e = moe::launch_tc_prep(sh, T, ws, s);
+      tr.mark(10);
+    }
+    if (e == cudaSuccess) {
+      e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 0, h->n_sm, s);
+      tr.mark(11);
+    }
+    if (e == cudaSuccess) {
+      e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 1, h->n_sm, s);
+      tr.mark(12);
+    }
+    if (e == cudaSuccess) {
+      e = moe::launch_combine(sh, T, ws, y, accumulate, s);
+      tr.mark(6);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (tensor-core path)");
   } else {
     e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
     if (e == cudaSuccess) {
@@ -428,6 +462,7 @@ void moe_destroy(moe_layer_t* h) {
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
   free_trace(h);
+  moe::tc_destroy_maps(h->tc);
   cudaFree(h->ws_base);
   if (cur >= 0) cudaSetDevice(cur);
   delete h;

@@ -29,6 +29,10 @@ struct Workspace {
   int32_t* dev_err;  // device error word (bounded waits that gave up)
   int32_t* dslot;    // [3][32] small-batch slot table: expert, first position, entries
   unsigned long long* gbar;  // grid barrier counter of the small-batch kernel (monotonic)
+  __half* x16;       // [Tm*k + Tm][H]    f16 activation rows of the tensor-core path
+  __half* h16;       // [Tm*k + Tm][Imax] f16 SwiGLU rows of the tensor-core path
+  int4* chunks;      // routed chunks of <= 64 plan rows: {first row, rows, expert, 0}
+  int32_t* n_rchunks;  // [1] number of routed chunks
   int hstride;       // row stride of hbuf in floats (>= Imax, multiple of 1024)
 };
 
@@ -40,7 +44,11 @@ struct Shape {
 }  // namespace moe
 
 // Phase ids of the trace API (a call records only the phases it runs).
-#define MOE_N_PHASES 10
+#define MOE_N_PHASES 13
+
+namespace moe {
+struct TcMaps;  // TMA tensor maps of the tensor-core grouped GEMM (tc_gemm.cu)
+}
 
 struct moe_layer {
   moe_config_t cfg;
@@ -53,6 +61,7 @@ struct moe_layer {
   char err[512];
   int n_sm;
   unsigned long long decode_calls;  // small-batch launches so far (grid barrier targets)
+  moe::TcMaps* tc;                  // NULL when the shape does not fit the tensor-core path
   // phase tracing: trace_cap calls x (MOE_N_PHASES + 1) events, and per call
   // the phase id recorded after each launched phase
   cudaEvent_t* trace_ev;
@@ -98,6 +107,18 @@ cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T,
 // y = (acc ? y : 0) + sum_j w_tj * o_(t,j) + o_shared_t.
 cudaError_t launch_combine(const Shape& sh, int T, const Workspace& ws, float* y,
                            int accumulate, cudaStream_t s);
+
+// Tensor-core grouped GEMM path (tc_gemm.cu): any T, shapes with H, I and
+// the shared I multiples of 256.
+bool tc_path_ok(const Shape& sh);
+size_t tc_max_chunks(int Tm, int k, int E);
+TcMaps* tc_create_maps(const moe_weights_t& w, const Shape& sh, const Workspace& ws, int Tm);
+void tc_destroy_maps(TcMaps* m);
+// routed chunk list + f16 activation rows
+cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStream_t s);
+// mode 0: gate/up -> h16; mode 1: down -> obuf
+cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Workspace& ws, int mode,
+                           int n_sm, cudaStream_t s);
 
 // Fused small-batch path (T <= 4, T*k <= 32).  When `marker.fn` is set
 // (phase tracing), the kernels are launched without the programmatic-

@@ -1,0 +1,583 @@
+// Tensor-core grouped GEMM of the routed experts for multi-token batches
+// (prefill, and any batch the small-batch kernels do not take).
+//
+// What it computes ("GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri
+// hierarchy": N2 per-expert gate/up/down int4 tensors with grouped scales,
+// N4 each expert runs once over the rows routed to it; "G2 - native GLM-5.2
+// correctness spine": dequantise, multiply, accumulate in f32):
+//   gate/up pass: for every expert e and its plan rows P_e,
+//       h[p][r] = SiLU(sum_k Wg[e][r][k] x[p][k]) * (sum_k Wu[e][r][k] x[p][k])
+//   down pass:   o[p][m] = sum_r Wd[e][m][r] h[p][r]
+// the shared expert runs the same way over all T tokens (rows T*k + t).
+//
+// Precision: the tensor cores multiply f16 operands.  The dequantised weight
+// (u - 8) * s is rounded once to f16 (relative error <= 2^-11); the
+// activations are rounded to f16 (bf16 inputs are exact); products are
+// accumulated in f32 in tensor memory.
+//
+// Structure (one persistent CTA per SM, 14 warps):
+//   warp 12      TMA producer: per 256-wide K stage, the int4 tile of 128
+//                weight rows (128-byte swizzled), its f16 scales and up to 64
+//                activation rows (four 64-wide K slabs, 128-byte swizzled)
+//                into a 4-deep shared-memory ring.
+//   warps 0..7   dequantisers: each thread owns one weight row (TMEM lane)
+//                and one 32-wide scale group per slab, turns the 32 nibbles
+//                into f16 (u - 8) * s with LOP3 + HSUB2/HFMA2 + HMUL2 and
+//                stores them to a TMEM A buffer (3 buffers of one stage).
+//   warp 13      MMA issuer: tcgen05.mma kind::f16, M = 128, N = tokens
+//                rounded to 16, A from TMEM, B from shared memory, D (f32)
+//                in one of two TMEM accumulators.
+//   warps 8..11  epilogue: TMEM -> registers; gate/up: SwiGLU and the f16
+//                activation row for the down pass; down: f32 output rows.
+// Every wait is bounded; a wait that gives up sets the device error word and
+// the role stops.
+//
+// Weight rows of one gate/up item: 64 gate rows r0..r0+63 (TMEM lanes 0..63)
+// and the matching 64 up rows (lanes 64..127), so SiLU(g) * u pairs lanes
+// l and l + 64.  K order: the dequantiser emits the nibbles of a 32-bit word
+// as the f16 pairs (0,4) (1,5) (2,6) (3,7); the activation rows are stored
+// with the same order inside every 8 elements so that the contraction pairs
+// matching elements (an order inside the dot product only).
+#include <string.h>
+
+#include <new>
+
+#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+struct TcMaps {
+  CUtensorMap gu_q[2][2];  // [routed, shared][gate, up] int4 rows, box 128 B x 64 rows
+  CUtensorMap gu_s[2][2];  // scales, box 8 x 64
+  CUtensorMap dn_q[2];     // [routed, shared] down int4 rows, box 128 B x 128 rows
+  CUtensorMap dn_s[2];     // scales, box 8 x 128
+  CUtensorMap x16;         // [R][H] f16 activations, box 64 x 16
+  CUtensorMap h16;         // [R][Imax] f16 SwiGLU rows, box 64 x 16
+};
+
+namespace tc {
+
+constexpr int kStages = 4;
+constexpr int kKS = 256;                     // K per stage
+constexpr int kNMax = 64;                    // tokens per chunk
+constexpr int kAQBytes = 128 * 128;          // int4 tile: 128 rows x 256 nibbles
+constexpr int kASBytes = 128 * 16;           // 8 f16 scales per row
+constexpr int kSlabBytes = kNMax * 128;      // 64 rows x 64 f16
+constexpr int kBBytes = 4 * kSlabBytes;
+constexpr int kStageBytes = kAQBytes + kASBytes + kBBytes;  // 51200, multiple of 1024
+constexpr int kXchStride = 65;
+constexpr int kDqWarps = 8, kEpWarps = 4;
+constexpr int kWarpProd = kDqWarps + kEpWarps, kWarpMma = kWarpProd + 1;
+constexpr int kThreads = (kWarpMma + 1) * 32;  // 448
+constexpr int kABufs = 3;
+constexpr uint32_t kTmemCols = 512;  // D: 2 x 64 columns, A: 3 x 128 columns
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNMax * kXchStride * 4 + 256;
+
+struct Args {
+  CUtensorMap aq[2][2];  // [routed, shared][gate, up] (down: [..][0])
+  CUtensorMap as[2][2];
+  CUtensorMap b;
+  Workspace ws;
+  int T, N, H, I, Is, Imax;
+  int mt_r, mt_s;    // M tiles per chunk (routed, shared)
+  int ks_r, ks_s;    // K stages per item
+  int n_sh_chunks;
+};
+
+struct Item {
+  int row0, n, e, mt;
+};
+
+__device__ __forceinline__ Item decode_item(const Args& a, int i) {
+  Item t;
+  const int n_sh_items = a.n_sh_chunks * a.mt_s;
+  if (i < n_sh_items) {
+    const int c = i / a.mt_s;
+    t.mt = i - c * a.mt_s;
+    t.row0 = a.N + kNMax * c;
+    t.n = min(kNMax, a.T - kNMax * c);
+    t.e = -1;
+  } else {
+    const int j = i - n_sh_items;
+    const int c = j / a.mt_r;
+    t.mt = j - c * a.mt_r;
+    const int4 ch = a.ws.chunks[c];
+    t.row0 = ch.x;
+    t.n = ch.y;
+    t.e = ch.z;
+  }
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lop(uint32_t v, uint32_t mask) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(0x64006400u));
+  return r;
+}
+__device__ __forceinline__ uint32_t h2u(__half2 h) {
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+__device__ __forceinline__ __half2 u2h(uint32_t u) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return h;
+}
+
+// One 32-bit word of 8 nibbles -> four f16 pairs (u-8)*s, order (0,4) (1,5)
+// (2,6) (3,7).  1024 + u and 1024 + 16u are exact in f16; subtracting 1032,
+// or scaling by 1/16 and subtracting 72, leaves u - 8 exactly; the multiply
+// by the scale rounds once.
+__device__ __forceinline__ void dq_word_f16(uint32_t v, __half2 s2, uint32_t* out) {
+  const __half2 k1032 = u2h(0x64086408u), k16 = u2h(0x2C002C00u), km72 = u2h(0xD480D480u);
+  const uint32_t v8 = v >> 8;
+  const __half2 a = __hsub2(u2h(lop(v, 0x000F000Fu)), k1032);
+  const __half2 b = __hfma2(u2h(lop(v, 0x00F000F0u)), k16, km72);
+  const __half2 c = __hsub2(u2h(lop(v8, 0x000F000Fu)), k1032);
+  const __half2 d = __hfma2(u2h(lop(v8, 0x00F000F0u)), k16, km72);
+  out[0] = h2u(__hmul2(a, s2));
+  out[1] = h2u(__hmul2(b, s2));
+  out[2] = h2u(__hmul2(c, s2));
+  out[3] = h2u(__hmul2(d, s2));
+}
+
+// position of element e (0..7) inside its group of 8 in the f16 rows
+__device__ __forceinline__ int kpos8(int r) { return (r & ~7) | ((r & 3) << 1) | ((r >> 2) & 1); }
+
+template <int MODE>  // 0: gate/up, 1: down
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Args a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* stages = smem;
+  float* xch = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xch + kNMax * kXchStride);
+  uint64_t* sfull = bars;
+  uint64_t* sempty = bars + kStages;
+  uint64_t* afull = sempty + kStages;
+  uint64_t* aempty = afull + kABufs;
+  uint64_t* dfull = aempty + kABufs;
+  uint64_t* dempty = dfull + 2;
+  uint64_t* drain = dempty + 2;
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* err = a.ws.dev_err;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(sfull + s), 1);
+      mbar_init(smem_u32(sempty + s), kDqWarps + 1);
+    }
+    for (int b = 0; b < kABufs; ++b) {
+      mbar_init(smem_u32(afull + b), kDqWarps);
+      mbar_init(smem_u32(aempty + b), 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(smem_u32(dfull + d), 1);
+      mbar_init(smem_u32(dempty + d), kEpWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tbase_s), kTmemCols);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *tbase_s;
+
+  const int total = a.n_sh_chunks * a.mt_s + *a.ws.n_rchunks * a.mt_r;
+
+  if (warp == kWarpProd) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&a.b);
+      uint32_t it = 0;
+      bool failed = false;
+      for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
+        const Item t = decode_item(a, i);
+        const int sh = t.e < 0 ? 1 : 0;
+        const int KS = sh ? a.ks_s : a.ks_r;
+        const int nb = (t.n + 15) >> 4;
+        int ya;
+        uint32_t bytes;
+        if (MODE == 0) {
+          ya = (sh ? 0 : t.e * a.I) + 64 * t.mt;
+        } else {
+          ya = (sh ? 0 : t.e * a.H) + 128 * t.mt;
+        }
+        bytes = kAQBytes + kASBytes + nb * 4 * 2048;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(smem_u32(sempty + s), ((it / kStages) & 1) ^ 1, err)) {
+            failed = true;
+            break;
+          }
+          fence_proxy_async_smem();
+          const uint32_t full = smem_u32(sfull + s);
+          const uint32_t base = smem_u32(stages + s * kStageBytes);
+          mbar_arrive_expect_tx(full, bytes);
+          if (MODE == 0) {
+            tma_load_2d(base, &a.aq[sh][0], ks * 128, ya, full);
+            tma_load_2d(base + 8192, &a.aq[sh][1], ks * 128, ya, full);
+            tma_load_2d(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full);
+            tma_load_2d(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full);
+          } else {
+            tma_load_2d(base, &a.aq[sh][0], ks * 128, ya, full);
+            tma_load_2d(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full);
+          }
+          const uint32_t bb = base + kAQBytes + kASBytes;
+          for (int j = 0; j < 4; ++j)
+            for (int b = 0; b < nb; ++b)
+              tma_load_2d(bb + j * kSlabBytes + b * 2048, &a.b, ks * kKS + 64 * j,
+                          t.row0 + 16 * b, full);
+        }
+      }
+      // let copies in flight land before the CTA exits
+      const uint32_t n_wait = it < kStages ? it : kStages;
+      for (uint32_t j = it - n_wait; j < it; ++j)
+        mbar_wait(smem_u32(sfull + j % kStages), (j / kStages) & 1, err);
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, ic = 0;
+      bool failed = false;
+      for (int i = blockIdx.x; i < total && !failed; i += gridDim.x, ++ic) {
+        const Item t = decode_item(a, i);
+        const int KS = t.e < 0 ? a.ks_s : a.ks_r;
+        const uint32_t idesc = idesc_f16(128, ((t.n + 15) >> 4) * 16);
+        const int d = ic & 1;
+        if (!mbar_wait(smem_u32(dempty + d), ((ic >> 1) & 1) ^ 1, err)) break;
+        fence_after_sync();
+        const uint32_t dt = tb + 64 * d;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kStages, ab = it % kABufs;
+          if (!mbar_wait(smem_u32(sfull + s), (it / kStages) & 1, err) ||
+              !mbar_wait(smem_u32(afull + ab), (it / kABufs) & 1, err)) {
+            failed = true;
+            break;
+          }
+          fence_after_sync();
+          const uint32_t at = tb + 128 + 128 * ab;
+          const uint32_t bb = smem_u32(stages + s * kStageBytes + kAQBytes + kASBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(dt, at + 32 * j + 8 * kk, sdesc_sw128(bb + j * kSlabBytes + 32 * kk), idesc,
+                     (ks | j | kk) != 0);
+          mma_commit(smem_u32(aempty + ab));
+          mma_commit(smem_u32(sempty + s));
+        }
+        if (failed) break;
+        mma_commit(smem_u32(dfull + d));
+      }
+      // every MMA this thread issued has completed once the drain barrier flips
+      mma_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0, err);
+    }
+  } else if (warp < kDqWarps) {
+    // ---------------- dequantisers ----------------
+    const int q = warp & 3, h = warp >> 2;
+    const int R = 32 * q + lane;  // weight row of the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    uint32_t it = 0;
+    bool failed = false;
+    for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
+      const Item t = decode_item(a, i);
+      const int KS = t.e < 0 ? a.ks_s : a.ks_r;
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kStages, ab = it % kABufs;
+        if (!mbar_wait(smem_u32(sfull + s), (it / kStages) & 1, err)) {
+          failed = true;
+          break;
+        }
+        const unsigned char* st = stages + s * kStageBytes;
+        const uint4 sc = *reinterpret_cast<const uint4*>(st + kAQBytes + R * 16);
+        uint4 w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int g = 2 * j + h;
+          w[j] = *reinterpret_cast<const uint4*>(st + R * 128 + ((g ^ (R & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sempty + s));
+        if (!mbar_wait(smem_u32(aempty + ab), ((it / kABufs) & 1) ^ 1, err)) {
+          failed = true;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t at = tb + lane_base + 128 + 128 * ab + 16 * h;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t sw = j == 0 ? sc.x : j == 1 ? sc.y : j == 2 ? sc.z : sc.w;
+          const uint32_t sbits = h ? (sw >> 16) : (sw & 0xFFFFu);
+          const __half2 s2 = u2h(sbits | (sbits << 16));
+          uint32_t v[16];
+          dq_word_f16(w[j].x, s2, v + 0);
+          dq_word_f16(w[j].y, s2, v + 4);
+          dq_word_f16(w[j].z, s2, v + 8);
+          dq_word_f16(w[j].w, s2, v + 12);
+          tmem_st16(at + 32 * j, v);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(afull + ab));
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 8..11, TMEM lane quadrant warp % 4) ----------------
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    uint32_t ic = 0;
+    for (int i = blockIdx.x; i < total; i += gridDim.x, ++ic) {
+      const Item t = decode_item(a, i);
+      const int d = ic & 1;
+      if (!mbar_wait(smem_u32(dfull + d), (ic >> 1) & 1, err)) break;
+      fence_after_sync();
+      uint32_t v[4][16];
+      const int nch = (t.n + 15) >> 4;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < nch) tmem_ld16(tb + lane_base + 64 * d + 16 * c, v[c]);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(dempty + d));
+      if (MODE == 0) {
+        if (q >= 2) {
+          float* xr = xch + (32 * (q - 2) + lane) * kXchStride;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < t.n) xr[c] = __uint_as_float(v[c >> 4][c & 15]);
+        }
+        named_sync(1, kEpWarps * 32);
+        if (q < 2) {
+          const int r = 64 * t.mt + 32 * q + lane;
+          const float* xr = xch + (32 * q + lane) * kXchStride;
+          __half* hrow = a.ws.h16 + static_cast<size_t>(t.row0) * a.Imax + kpos8(r);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < t.n) {
+              const float g = __uint_as_float(v[c >> 4][c & 15]);
+              const float u = xr[c];
+              const float silu = g / (1.0f + expf(-g));
+              hrow[static_cast<size_t>(c) * a.Imax] = __float2half_rn(silu * u);
+            }
+        }
+        named_sync(1, kEpWarps * 32);
+      } else {
+        const int m = 128 * t.mt + 32 * q + lane;
+        float* orow = a.ws.obuf + static_cast<size_t>(t.row0) * a.H + m;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < t.n) orow[static_cast<size_t>(c) * a.H] = __uint_as_float(v[c >> 4][c & 15]);
+      }
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tb, kTmemCols);
+  }
+}
+
+// Routed chunk list (warp 0 of block 0) and the f16 activation rows: row p <
+// T*k holds token perm[p] / k, row T*k + t token t, each in the 8-element
+// order of the dequantised weights.
+__global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, Workspace ws) {
+  const int N = T * sh.k, H = sh.H;
+  const int row = blockIdx.x;
+  if (row == 0 && threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int b = 0; b < sh.E; b += 32) {
+      const int e = b + lane;
+      const int n = e < sh.E ? ws.counts[e] : 0;
+      const int nc = (n + kNMax - 1) / kNMax;
+      int incl = nc;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      const int pos = carry + incl - nc;
+      const int off = e < sh.E ? ws.offsets[e] : 0;
+      for (int c = 0; c < nc; ++c)
+        ws.chunks[pos + c] = make_int4(off + kNMax * c, min(kNMax, n - kNMax * c), e, 0);
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) *ws.n_rchunks = carry;
+  }
+  const int tok = row < N ? ws.perm[row] / sh.k : row - N;
+  const float4* src = reinterpret_cast<const float4*>(ws.xf + static_cast<size_t>(tok) * H);
+  uint4* dst = reinterpret_cast<uint4*>(ws.x16 + static_cast<size_t>(row) * H);
+  for (int o = threadIdx.x; o < H / 8; o += blockDim.x) {
+    const float4 lo = src[2 * o], hi = src[2 * o + 1];
+    uint4 r;
+    r.x = h2u(__floats2half2_rn(lo.x, hi.x));
+    r.y = h2u(__floats2half2_rn(lo.y, hi.y));
+    r.z = h2u(__floats2half2_rn(lo.z, hi.z));
+    r.w = h2u(__floats2half2_rn(lo.w, hi.w));
+    dst[o] = r;
+  }
+}
+
+// ---- host side --------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D map over rows x cols elements (row stride = cols * esize bytes).
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+               uint64_t cols, uint64_t rows, uint32_t box_c, uint32_t box_r, bool swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esize};
+  const cuuint32_t box[2] = {box_c, box_r};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+int imax_of(const Shape& sh) { return sh.n_shared && sh.Is > sh.I ? sh.Is : sh.I; }
+
+}  // namespace tc
+
+bool tc_path_ok(const Shape& sh) {
+  if (sh.H % 256 != 0 || sh.I % 256 != 0) return false;
+  if (sh.n_shared && sh.Is % 256 != 0) return false;
+  return true;
+}
+
+size_t tc_max_chunks(int Tm, int k, int E) {
+  return static_cast<size_t>(Tm) * k / tc::kNMax + E + 1;
+}
+
+TcMaps* tc_create_maps(const moe_weights_t& w, const Shape& sh, const Workspace& ws, int Tm) {
+  using namespace tc;
+  if (!tc_path_ok(sh)) return nullptr;
+  TcMaps* m = new (std::nothrow) TcMaps;
+  if (!m) return nullptr;
+  memset(m, 0, sizeof(TcMaps));
+  const uint64_t H = sh.H, I = sh.I, E = sh.E, Is = sh.Is;
+  const uint64_t R = static_cast<uint64_t>(Tm) * sh.k + Tm;
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, U16 = CU_TENSOR_MAP_DATA_TYPE_UINT16,
+             F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  bool ok = true;
+  ok = ok && encode_2d(&m->gu_q[0][0], w.gate_q, U8, 1, H / 2, E * I, 128, 64, true);
+  ok = ok && encode_2d(&m->gu_q[0][1], w.up_q, U8, 1, H / 2, E * I, 128, 64, true);
+  ok = ok && encode_2d(&m->gu_s[0][0], w.gate_s, U16, 2, H / 32, E * I, 8, 64, false);
+  ok = ok && encode_2d(&m->gu_s[0][1], w.up_s, U16, 2, H / 32, E * I, 8, 64, false);
+  ok = ok && encode_2d(&m->dn_q[0], w.down_q, U8, 1, I / 2, E * H, 128, 128, true);
+  ok = ok && encode_2d(&m->dn_s[0], w.down_s, U16, 2, I / 32, E * H, 8, 128, false);
+  if (sh.n_shared) {
+    ok = ok && encode_2d(&m->gu_q[1][0], w.sh_gate_q, U8, 1, H / 2, Is, 128, 64, true);
+    ok = ok && encode_2d(&m->gu_q[1][1], w.sh_up_q, U8, 1, H / 2, Is, 128, 64, true);
+    ok = ok && encode_2d(&m->gu_s[1][0], w.sh_gate_s, U16, 2, H / 32, Is, 8, 64, false);
+    ok = ok && encode_2d(&m->gu_s[1][1], w.sh_up_s, U16, 2, H / 32, Is, 8, 64, false);
+    ok = ok && encode_2d(&m->dn_q[1], w.sh_down_q, U8, 1, Is / 2, H, 128, 128, true);
+    ok = ok && encode_2d(&m->dn_s[1], w.sh_down_s, U16, 2, Is / 32, H, 8, 128, false);
+  }
+  ok = ok && encode_2d(&m->x16, ws.x16, F16, 2, H, R, 64, 16, true);
+  ok = ok && encode_2d(&m->h16, ws.h16, F16, 2, imax_of(sh), R, 64, 16, true);
+  if (!ok) {
+    delete m;
+    return nullptr;
+  }
+  return m;
+}
+
+void tc_destroy_maps(TcMaps* m) { delete m; }
+
+cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStream_t s) {
+  const int rows = T * sh.k + (sh.n_shared ? T : 0);
+  tc::tc_prep_kernel<<<rows, 256, 0, s>>>(sh, T, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Workspace& ws, int mode,
+                           int n_sm, cudaStream_t s) {
+  using namespace tc;
+  Args a;
+  memset(&a, 0, sizeof(a));
+  a.ws = ws;
+  a.T = T;
+  a.N = T * sh.k;
+  a.H = sh.H;
+  a.I = sh.I;
+  a.Is = sh.n_shared ? sh.Is : sh.I;
+  a.Imax = imax_of(sh);
+  a.n_sh_chunks = sh.n_shared ? (T + kNMax - 1) / kNMax : 0;
+  if (mode == 0) {
+    a.aq[0][0] = m.gu_q[0][0];
+    a.aq[0][1] = m.gu_q[0][1];
+    a.as[0][0] = m.gu_s[0][0];
+    a.as[0][1] = m.gu_s[0][1];
+    a.aq[1][0] = m.gu_q[1][0];
+    a.aq[1][1] = m.gu_q[1][1];
+    a.as[1][0] = m.gu_s[1][0];
+    a.as[1][1] = m.gu_s[1][1];
+    a.b = m.x16;
+    a.mt_r = sh.I / 64;
+    a.mt_s = a.Is / 64;
+    a.ks_r = a.ks_s = sh.H / kKS;
+  } else {
+    a.aq[0][0] = m.dn_q[0];
+    a.as[0][0] = m.dn_s[0];
+    a.aq[1][0] = m.dn_q[1];
+    a.as[1][0] = m.dn_s[1];
+    a.b = m.h16;
+    a.mt_r = a.mt_s = sh.H / 128;
+    a.ks_r = sh.I / kKS;
+    a.ks_s = a.Is / kKS;
+  }
+  const void* fn = mode == 0 ? reinterpret_cast<const void*>(tc_gemm_kernel<0>)
+                             : reinterpret_cast<const void*>(tc_gemm_kernel<1>);
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[mode]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[mode] = true;
+  }
+  if (mode == 0)
+    tc_gemm_kernel<0><<<n_sm, kThreads, kSmemBytes, s>>>(a);
+  else
+    tc_gemm_kernel<1><<<n_sm, kThreads, kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -230,14 +230,76 @@ def test_trace_phases(m):
     h.forward(gen_activations(wl, 20, call=1).to(DEV))
     h.forward(gen_activations(wl, 3, call=2).to(DEV))
     names, rows = m.moe_trace_read(h.h, 3)
-    assert len(rows) == 3 and len(names) == 10
+    assert len(rows) == 3 and len(names) == 13
     small = {n for n, v in zip(names, rows[0]) if v > 0}
-    general = {n for n, v in zip(names, rows[1]) if v > 0}
+    tc = {n for n, v in zip(names, rows[1]) if v > 0}
     assert small == {"decode_fused"}
-    assert {"prep", "router_logits", "select", "plan", "gate_up", "down", "combine"} <= general
+    assert tc == {"prep", "router_logits", "select", "plan", "tc_prep", "tc_gate_up", "tc_down",
+                  "combine"}
     batch = {n for n, v in zip(names, rows[2]) if v > 0}
     assert batch == {"decode_router_gate_up", "decode_down_combine"}
     m.moe_trace_enable(h.h, 0)
+    h.close()
+    # intermediate size not a multiple of 256: the SIMT general path
+    wl, L, h = _tiny_handle(m, 32)
+    m.moe_trace_enable(h.h, 1)
+    h.forward(gen_activations(wl, 20, call=1).to(DEV))
+    names, rows = m.moe_trace_read(h.h, 1)
+    general = {n for n, v in zip(names, rows[0]) if v > 0}
+    assert general == {"prep", "router_logits", "select", "plan", "gate_up", "down", "combine"}
+    m.moe_trace_enable(h.h, 0)
+    h.close()
+
+
+# ------------------------------------------------ tensor-core grouped GEMM ---
+
+TC_SHAPES = [
+    # H, I, E, k, n_group, topk_group, n_shared, shared_inter (0: = I)
+    (512, 256, 16, 4, 4, 2, 1, 0),
+    (1024, 512, 8, 2, 2, 1, 1, 768),   # shared expert wider than the routed ones
+    (256, 256, 8, 2, 2, 1, 0, 0),      # no shared expert
+    (768, 256, 32, 6, 8, 4, 1, 512),
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("T", [5, 40, 150])
+def test_tc_grouped_gemm(m, shape, T):
+    H, I, E, k, ng, tg, ns, Is = shape
+    sh = LayerShape(H, I, E, k, ng, tg, 2.5, n_shared=ns, shared_inter=Is)
+    wl = Workload("tc", sh, T, 1, "bf16" if T % 2 else "f32", "zipf", 7700 + H + I + E + T)
+    L = gen_layer(wl, device=DEV)
+    x = gen_activations(wl, T, call=0)
+    _run_full(m, wl, L, x, max_tokens=T + 3)
+
+
+def test_tc_multi_chunk_experts(m):
+    """Experts with more than 64 rows (several chunks) and a 300-token
+    shared expert (five chunks, the last one ragged)."""
+    sh = LayerShape(512, 256, 4, 2, 1, 1, 2.5)
+    wl = Workload("tc_chunks", sh, 300, 1, "bf16", "zipf", 7801)
+    L = gen_layer(wl, device=DEV)
+    x = gen_activations(wl, 300, call=0)
+    _, plan, _ = _run_full(m, wl, L, x, sample=list(range(0, 300, 7)) + [299])
+    assert plan.counts.cpu().numpy().max() > 128
+
+
+def test_tc_rmsnorm_residual(m):
+    sh = LayerShape(512, 512, 16, 4, 4, 2, 2.5)
+    wl = Workload("tc_resid", sh, 24, 1, "f32", "zipf", 7802, rmsnorm_eps=1e-5)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 64)
+    gamma = gen_norm_weight(wl, 0)
+    for T in (9, 64):
+        x0 = (gen_activations(wl, T, call=T) * 2.0).float()
+        xd = x0.to(DEV)
+        h.forward(xd, y=xd, gamma=gamma.to(DEV), eps=RMS_EPS, accumulate=True)
+        torch.cuda.synchronize()
+        assert m.moe_device_status(h.h) == 0
+        y_o, _, _, _ = oracle_layer(wl, 0, router_of(wl), x0.numpy(), range(T), eps=RMS_EPS,
+                                    gamma=gamma.numpy(), resid=x0.numpy())
+        err = resid_err_per_token(xd.cpu().numpy(), y_o, x0.numpy())
+        assert err.max() <= TOL
     h.close()
 
 
