@@ -197,21 +197,22 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
 
 # ------------------------------------------------------------- workloads ----
 
-def workload_key(wl, experts=None):
-    return f"{wl.name}_E{experts}" if experts else wl.name
+def workload_key(wl, experts=None, tokens=None):
+    key = f"{wl.name}_E{experts}" if experts else wl.name
+    return f"{key}_T{tokens}" if tokens else key
 
 
-def make_workload(name, experts=None, calls=None):
+def make_workload(name, experts=None, calls=None, tokens=None):
     from workloads import CONFIGS
     from workloads.configs import LayerShape, Workload
     wl = CONFIGS[name]
-    if experts or calls:
+    if experts or calls or tokens:
         sh = wl.shape
         if experts:
             sh = LayerShape(sh.hidden, sh.inter, experts, sh.top_k, sh.n_group, sh.topk_group,
                             sh.routed_scaling_factor, sh.n_shared, sh.shared_inter,
                             sh.group_size)
-        wl = Workload(wl.name, sh, wl.tokens_per_call, calls or wl.calls, wl.x_dtype,
+        wl = Workload(wl.name, sh, tokens or wl.tokens_per_call, calls or wl.calls, wl.x_dtype,
                       wl.bias_kind, wl.seed, wl.layers, wl.correlated, wl.rmsnorm_eps,
                       wl.zipf_s)
     return wl
@@ -427,9 +428,11 @@ def main():
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
     ap.add_argument("--calls", type=int, default=None, help="override calls per step")
     ap.add_argument("--layers", type=int, default=None, help="override stacked layers")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override tokens per call (profiling only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    wl = make_workload(args.workload, args.experts, args.calls)
+    wl = make_workload(args.workload, args.experts, args.calls, args.tokens)
 
     if args.impl == "reference":
         run_reference(args, wl)
@@ -539,7 +542,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": dominant,
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "traffic": ncu_traffic(dominant, workload_key(wl, args.experts)),
+                         "traffic": ncu_traffic(dominant, workload_key(wl, args.experts, args.tokens)),
                          "algorithmic_bytes_per_launch": kb,
                          "avg_launch_us": round(1000 * per_launch_ms, 3),
                          "duration_source": "CUDA events between the kernels in a traced pass "

@@ -15,26 +15,31 @@
 // activations are rounded to f16 (bf16 inputs are exact); products are
 // accumulated in f32 in tensor memory.
 //
-// Structure (one persistent CTA per SM, 14 warps):
-//   warp 12      TMA producer: per 256-wide K stage, the int4 tile of 128
-//                weight rows (128-byte swizzled), its f16 scales and up to 64
-//                activation rows (four 64-wide K slabs, 128-byte swizzled)
-//                into a 4-deep shared-memory ring.
-//   warps 0..7   dequantisers: each thread owns one weight row (TMEM lane)
-//                and one 32-wide scale group per slab, turns the 32 nibbles
-//                into f16 (u - 8) * s with LOP3 + HSUB2/HFMA2 + HMUL2 and
-//                stores them to a TMEM A buffer (3 buffers of one stage).
-//   warp 13      MMA issuer: tcgen05.mma kind::f16, M = 128, N = tokens
+// Structure (one persistent CTA per SM, 23 warps):
+//   warp 20      TMA producer of the weights: per 256-wide K stage, the int4
+//                tile of 128 weight rows (128-byte swizzled) and its f16
+//                scales, into a 7-deep shared-memory ring.
+//   warp 21      TMA producer of the activations: per stage up to 64 f16
+//                rows (four 64-wide K slabs, 128-byte swizzled), 3-deep ring.
+//   warps 0..15  dequantisers: each thread owns one weight row (TMEM lane)
+//                and one 64-wide K slab of every stage (two scale groups),
+//                turns the 64 nibbles into f16 (u - 8) * s with LOP3 +
+//                HSUB2/HFMA2 + HMUL2 and stores them to a TMEM A buffer
+//                (3 buffers of one stage).
+//   warp 22      MMA issuer: tcgen05.mma kind::f16, M = 128, N = tokens
 //                rounded to 16, A from TMEM, B from shared memory, D (f32)
 //                in one of two TMEM accumulators.
-//   warps 8..11  epilogue: TMEM -> registers; gate/up: SwiGLU and the f16
+//   warps 16..19 epilogue: TMEM -> registers; gate/up: SwiGLU and the f16
 //                activation row for the down pass; down: f32 output rows.
+// Weights and scales are loaded with the L2 evict-first policy (read once),
+// activation rows with evict-last (every M tile of a chunk re-reads them).
 // Every wait is bounded; a wait that gives up sets the device error word and
 // the role stops.
 //
-// Weight rows of one gate/up item: 64 gate rows r0..r0+63 (TMEM lanes 0..63)
-// and the matching 64 up rows (lanes 64..127), so SiLU(g) * u pairs lanes
-// l and l + 64.  K order: the dequantiser emits the nibbles of a 32-bit word
+// Weight rows of one gate/up item: 64 gate rows r0..r0+63 and the matching
+// 64 up rows; TMEM lane 32q + l holds gate row r0 + 16q + l for l < 16 and
+// up row r0 + 16q + l - 16 for l >= 16, so SiLU(g) * u pairs lanes l and
+// l + 16 of one warp.  K order: the dequantiser emits the nibbles of a 32-bit word
 // as the f16 pairs (0,4) (1,5) (2,6) (3,7); the activation rows are stored
 // with the same order inside every 8 elements so that the contraction pairs
 // matching elements (an order inside the dot product only).
@@ -58,21 +63,22 @@ struct TcMaps {
 
 namespace tc {
 
-constexpr int kStages = 4;
+constexpr int kWStages = 7;                  // weight-tile ring depth
+constexpr int kBStages = 3;                  // activation-row ring depth
 constexpr int kKS = 256;                     // K per stage
 constexpr int kNMax = 64;                    // tokens per chunk
 constexpr int kAQBytes = 128 * 128;          // int4 tile: 128 rows x 256 nibbles
 constexpr int kASBytes = 128 * 16;           // 8 f16 scales per row
+constexpr int kWBytes = kAQBytes + kASBytes; // 18432, multiple of 1024
 constexpr int kSlabBytes = kNMax * 128;      // 64 rows x 64 f16
-constexpr int kBBytes = 4 * kSlabBytes;
-constexpr int kStageBytes = kAQBytes + kASBytes + kBBytes;  // 51200, multiple of 1024
-constexpr int kXchStride = 65;
-constexpr int kDqWarps = 8, kEpWarps = 4;
-constexpr int kWarpProd = kDqWarps + kEpWarps, kWarpMma = kWarpProd + 1;
-constexpr int kThreads = (kWarpMma + 1) * 32;  // 448
-constexpr int kABufs = 3;
+constexpr int kBBytes = 4 * kSlabBytes;      // 32768
+constexpr int kDqWarps = 16, kEpWarps = 4;
+constexpr int kWarpWProd = kDqWarps + kEpWarps, kWarpBProd = kWarpWProd + 1,
+              kWarpMma = kWarpBProd + 1;
+constexpr int kThreads = (kWarpMma + 1) * 32;  // 736
+constexpr int kABufs = kBStages;  // A buffers and B slots advance together
 constexpr uint32_t kTmemCols = 512;  // D: 2 x 64 columns, A: 3 x 128 columns
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNMax * kXchStride * 4 + 256;
+constexpr int kSmemBytes = 1024 + kBStages * kBBytes + kWStages * kWBytes + 512;
 
 struct Args {
   CUtensorMap aq[2][2];  // [routed, shared][gate, up] (down: [..][0])
@@ -143,22 +149,49 @@ __device__ __forceinline__ void dq_word_f16(uint32_t v, __half2 s2, uint32_t* ou
   out[3] = h2u(__hmul2(d, s2));
 }
 
+// One lane of a converged warp (the lowest active lane).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
+// Bounded wait whose outcome every lane of the warp shares, so that a warp
+// never splits before a warp-collective tcgen05 operation.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
 // position of element e (0..7) inside its group of 8 in the f16 rows
 __device__ __forceinline__ int kpos8(int r) { return (r & ~7) | ((r & 3) << 1) | ((r >> 2) & 1); }
+
+// Shared-memory row of the weight tile that TMEM lane L holds.  Gate/up: the
+// tile's rows 0..63 are gate rows, 64..127 the matching up rows; lane 32q + l
+// takes gate row 16q + l (l < 16) or up row 16q + l - 16 (l >= 16), so one
+// warp holds both halves of its 16 SwiGLU rows.  Down: the identity.
+template <int MODE>
+__device__ __forceinline__ int tile_row(int L) {
+  if (MODE == 1) return L;
+  const int q = L >> 5, l = L & 31;
+  return l < 16 ? 16 * q + l : 48 + 16 * q + l;
+}
 
 template <int MODE>  // 0: gate/up, 1: down
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Args a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char* stages = smem;
-  float* xch = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xch + kNMax * kXchStride);
-  uint64_t* sfull = bars;
-  uint64_t* sempty = bars + kStages;
-  uint64_t* afull = sempty + kStages;
-  uint64_t* aempty = afull + kABufs;
-  uint64_t* dfull = aempty + kABufs;
+  unsigned char* bring = smem;                                  // kBStages x kBBytes
+  unsigned char* wring = smem + kBStages * kBBytes;             // kWStages x kWBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wring + kWStages * kWBytes);
+  uint64_t* wfull = bars;
+  uint64_t* wempty = wfull + kWStages;
+  uint64_t* bfull = wempty + kWStages;
+  uint64_t* afull = bfull + kBStages;
+  uint64_t* sdone = afull + kABufs;  // MMAs of the stage done: its A buffer and B slot are free
+  uint64_t* dfull = sdone + kABufs;
   uint64_t* dempty = dfull + 2;
   uint64_t* drain = dempty + 2;
   uint32_t* tbase_s = reinterpret_cast<uint32_t*>(drain + 1);
@@ -167,13 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   int* err = a.ws.dev_err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(sfull + s), 1);
-      mbar_init(smem_u32(sempty + s), kDqWarps + 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(smem_u32(wfull + s), 1);
+      mbar_init(smem_u32(wempty + s), kDqWarps);
     }
+    for (int s = 0; s < kBStages; ++s) mbar_init(smem_u32(bfull + s), 1);
     for (int b = 0; b < kABufs; ++b) {
       mbar_init(smem_u32(afull + b), kDqWarps);
-      mbar_init(smem_u32(aempty + b), 1);
+      mbar_init(smem_u32(sdone + b), 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(smem_u32(dfull + d), 1);
@@ -193,99 +227,122 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   const int total = a.n_sh_chunks * a.mt_s + *a.ws.n_rchunks * a.mt_r;
 
-  if (warp == kWarpProd) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      prefetch_tmap(&a.b);
-      uint32_t it = 0;
-      bool failed = false;
-      for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
-        const Item t = decode_item(a, i);
-        const int sh = t.e < 0 ? 1 : 0;
-        const int KS = sh ? a.ks_s : a.ks_r;
-        const int nb = (t.n + 15) >> 4;
-        int ya;
-        uint32_t bytes;
-        if (MODE == 0) {
-          ya = (sh ? 0 : t.e * a.I) + 64 * t.mt;
-        } else {
-          ya = (sh ? 0 : t.e * a.H) + 128 * t.mt;
+  // The producer and MMA warps run converged: every lane takes the waits and
+  // one elected lane (the same lane each time) issues the copies, the MMAs
+  // and their commits.  Issuing from a converged warp keeps tcgen05.mma on
+  // the fast path; issuing from a lone divergent lane costs several times more.
+  if (warp == kWarpWProd) {
+    // ---------------- TMA producer: weight tiles ----------------
+    const uint64_t pol = policy_evict_first();  // weights are read once
+    uint32_t it = 0;
+    bool failed = false;
+    for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
+      const Item t = decode_item(a, i);
+      const int sh = t.e < 0 ? 1 : 0;
+      const int KS = sh ? a.ks_s : a.ks_r;
+      const int ya = MODE == 0 ? (sh ? 0 : t.e * a.I) + 64 * t.mt
+                               : (sh ? 0 : t.e * a.H) + 128 * t.mt;
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kWStages;
+        if (!warp_wait(smem_u32(wempty + s), ((it / kWStages) & 1) ^ 1, err)) {
+          failed = true;
+          break;
         }
-        bytes = kAQBytes + kASBytes + nb * 4 * 2048;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(smem_u32(sempty + s), ((it / kStages) & 1) ^ 1, err)) {
-            failed = true;
-            break;
-          }
+        if (elect_one()) {
           fence_proxy_async_smem();
-          const uint32_t full = smem_u32(sfull + s);
-          const uint32_t base = smem_u32(stages + s * kStageBytes);
-          mbar_arrive_expect_tx(full, bytes);
+          const uint32_t full = smem_u32(wfull + s);
+          const uint32_t base = smem_u32(wring + s * kWBytes);
+          mbar_arrive_expect_tx(full, kWBytes);
           if (MODE == 0) {
-            tma_load_2d(base, &a.aq[sh][0], ks * 128, ya, full);
-            tma_load_2d(base + 8192, &a.aq[sh][1], ks * 128, ya, full);
-            tma_load_2d(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full);
-            tma_load_2d(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full);
+            tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
+            tma_load_2d_hint(base + 8192, &a.aq[sh][1], ks * 128, ya, full, pol);
+            tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
+            tma_load_2d_hint(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full, pol);
           } else {
-            tma_load_2d(base, &a.aq[sh][0], ks * 128, ya, full);
-            tma_load_2d(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full);
+            tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
+            tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
           }
-          const uint32_t bb = base + kAQBytes + kASBytes;
+        }
+        __syncwarp();
+      }
+    }
+    // let copies in flight land before the CTA exits
+    const uint32_t n_wait = it < kWStages ? it : kWStages;
+    for (uint32_t j = it - n_wait; j < it; ++j)
+      warp_wait(smem_u32(wfull + j % kWStages), (j / kWStages) & 1, err);
+  } else if (warp == kWarpBProd) {
+    // ---------------- TMA producer: activation rows ----------------
+    if (elect_one()) prefetch_tmap(&a.b);
+    __syncwarp();
+    const uint64_t pol = policy_evict_last();  // activation rows are re-read by other CTAs
+    uint32_t it = 0;
+    bool failed = false;
+    for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
+      const Item t = decode_item(a, i);
+      const int KS = t.e < 0 ? a.ks_s : a.ks_r;
+      const int nb = (t.n + 15) >> 4;
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kBStages;
+        if (!warp_wait(smem_u32(sdone + s), ((it / kBStages) & 1) ^ 1, err)) {
+          failed = true;
+          break;
+        }
+        if (elect_one()) {
+          const uint32_t full = smem_u32(bfull + s);
+          const uint32_t base = smem_u32(bring + s * kBBytes);
+          mbar_arrive_expect_tx(full, nb * 4 * 2048);
           for (int j = 0; j < 4; ++j)
             for (int b = 0; b < nb; ++b)
-              tma_load_2d(bb + j * kSlabBytes + b * 2048, &a.b, ks * kKS + 64 * j,
-                          t.row0 + 16 * b, full);
+              tma_load_2d_hint(base + j * kSlabBytes + b * 2048, &a.b, ks * kKS + 64 * j,
+                               t.row0 + 16 * b, full, pol);
         }
+        __syncwarp();
       }
-      // let copies in flight land before the CTA exits
-      const uint32_t n_wait = it < kStages ? it : kStages;
-      for (uint32_t j = it - n_wait; j < it; ++j)
-        mbar_wait(smem_u32(sfull + j % kStages), (j / kStages) & 1, err);
     }
+    const uint32_t n_wait = it < kBStages ? it : kBStages;
+    for (uint32_t j = it - n_wait; j < it; ++j)
+      warp_wait(smem_u32(bfull + j % kBStages), (j / kBStages) & 1, err);
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      uint32_t it = 0, ic = 0;
-      bool failed = false;
-      for (int i = blockIdx.x; i < total && !failed; i += gridDim.x, ++ic) {
-        const Item t = decode_item(a, i);
-        const int KS = t.e < 0 ? a.ks_s : a.ks_r;
-        const uint32_t idesc = idesc_f16(128, ((t.n + 15) >> 4) * 16);
-        const int d = ic & 1;
-        if (!mbar_wait(smem_u32(dempty + d), ((ic >> 1) & 1) ^ 1, err)) break;
-        fence_after_sync();
-        const uint32_t dt = tb + 64 * d;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % kStages, ab = it % kABufs;
-          if (!mbar_wait(smem_u32(sfull + s), (it / kStages) & 1, err) ||
-              !mbar_wait(smem_u32(afull + ab), (it / kABufs) & 1, err)) {
-            failed = true;
-            break;
-          }
-          fence_after_sync();
-          const uint32_t at = tb + 128 + 128 * ab;
-          const uint32_t bb = smem_u32(stages + s * kStageBytes + kAQBytes + kASBytes);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(dt, at + 32 * j + 8 * kk, sdesc_sw128(bb + j * kSlabBytes + 32 * kk), idesc,
-                     (ks | j | kk) != 0);
-          mma_commit(smem_u32(aempty + ab));
-          mma_commit(smem_u32(sempty + s));
+    uint32_t it = 0, ic = 0;
+    bool failed = false;
+    for (int i = blockIdx.x; i < total && !failed; i += gridDim.x, ++ic) {
+      const Item t = decode_item(a, i);
+      const int KS = t.e < 0 ? a.ks_s : a.ks_r;
+      const uint32_t idesc = idesc_f16(128, ((t.n + 15) >> 4) * 16);
+      const int d = ic & 1;
+      if (!warp_wait(smem_u32(dempty + d), ((ic >> 1) & 1) ^ 1, err)) break;
+      fence_after_sync();
+      const uint32_t dt = tb + 64 * d;
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int sb = it % kBStages;  // B slot, A buffer and done barrier share the index
+        if (!warp_wait(smem_u32(bfull + sb), (it / kBStages) & 1, err) ||
+            !warp_wait(smem_u32(afull + sb), (it / kABufs) & 1, err)) {
+          failed = true;
+          break;
         }
-        if (failed) break;
-        mma_commit(smem_u32(dfull + d));
+        fence_after_sync();
+        const uint32_t at = tb + 128 + 128 * sb;
+        // descriptor of slab 0; later slabs / K steps add (byte offset >> 4) to the
+        // 14-bit start field, which stays below 2^14 inside shared memory
+        const uint64_t bd = sdesc_sw128(smem_u32(bring + sb * kBBytes));
+        if (elect_one()) {
+          mma_ts_stage16<kSlabBytes>(dt, at, bd, idesc, ks == 0);
+          mma_commit(smem_u32(sdone + sb));
+          if (ks == KS - 1) mma_commit(smem_u32(dfull + d));
+        }
+        __syncwarp();
       }
-      // every MMA this thread issued has completed once the drain barrier flips
-      mma_commit(smem_u32(drain));
-      mbar_wait(smem_u32(drain), 0, err);
     }
+    // every MMA this warp issued has completed once the drain barrier flips
+    if (elect_one()) mma_commit(smem_u32(drain));
+    __syncwarp();
+    warp_wait(smem_u32(drain), 0, err);
   } else if (warp < kDqWarps) {
     // ---------------- dequantisers ----------------
-    const int q = warp & 3, h = warp >> 2;
-    const int R = 32 * q + lane;  // weight row of the tile = TMEM lane
+    // warp w: TMEM lane quadrant w % 4, K slab w / 4 (groups 2j, 2j+1) of every stage
+    const int q = warp & 3, j = warp >> 2;
+    const int R = tile_row<MODE>(32 * q + lane);  // tile row of this thread's TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint32_t it = 0;
     bool failed = false;
@@ -293,93 +350,81 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Item t = decode_item(a, i);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kStages, ab = it % kABufs;
-        if (!mbar_wait(smem_u32(sfull + s), (it / kStages) & 1, err)) {
+        const int s = it % kWStages, ab = it % kABufs;
+        if (!warp_wait(smem_u32(wfull + s), (it / kWStages) & 1, err)) {
           failed = true;
           break;
         }
-        const unsigned char* st = stages + s * kStageBytes;
-        const uint4 sc = *reinterpret_cast<const uint4*>(st + kAQBytes + R * 16);
-        uint4 w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int g = 2 * j + h;
-          w[j] = *reinterpret_cast<const uint4*>(st + R * 128 + ((g ^ (R & 7)) << 4));
-        }
+        const unsigned char* st = wring + s * kWBytes;
+        const uint32_t sc = *reinterpret_cast<const uint32_t*>(st + kAQBytes + R * 16 + 4 * j);
+        const uint4 w0 = *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j) ^ (R & 7)) << 4));
+        const uint4 w1 =
+            *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j + 1) ^ (R & 7)) << 4));
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(sempty + s));
-        if (!mbar_wait(smem_u32(aempty + ab), ((it / kABufs) & 1) ^ 1, err)) {
+        if (lane == 0) mbar_arrive(smem_u32(wempty + s));
+        if (!warp_wait(smem_u32(sdone + ab), ((it / kABufs) & 1) ^ 1, err)) {
           failed = true;
           break;
         }
         fence_after_sync();
-        const uint32_t at = tb + lane_base + 128 + 128 * ab + 16 * h;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t sw = j == 0 ? sc.x : j == 1 ? sc.y : j == 2 ? sc.z : sc.w;
-          const uint32_t sbits = h ? (sw >> 16) : (sw & 0xFFFFu);
-          const __half2 s2 = u2h(sbits | (sbits << 16));
-          uint32_t v[16];
-          dq_word_f16(w[j].x, s2, v + 0);
-          dq_word_f16(w[j].y, s2, v + 4);
-          dq_word_f16(w[j].z, s2, v + 8);
-          dq_word_f16(w[j].w, s2, v + 12);
-          tmem_st16(at + 32 * j, v);
-        }
+        const __half2 s0 = u2h((sc & 0xFFFFu) | (sc << 16));
+        const __half2 s1 = u2h((sc >> 16) | (sc & 0xFFFF0000u));
+        uint32_t v[32];
+        dq_word_f16(w0.x, s0, v + 0);
+        dq_word_f16(w0.y, s0, v + 4);
+        dq_word_f16(w0.z, s0, v + 8);
+        dq_word_f16(w0.w, s0, v + 12);
+        dq_word_f16(w1.x, s1, v + 16);
+        dq_word_f16(w1.y, s1, v + 20);
+        dq_word_f16(w1.z, s1, v + 24);
+        dq_word_f16(w1.w, s1, v + 28);
+        tmem_st32(tb + lane_base + 128 + 128 * ab + 32 * j, v);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(afull + ab));
       }
     }
-  } else {
-    // ---------------- epilogue (warps 8..11, TMEM lane quadrant warp % 4) ----------------
+  } else if (warp < kDqWarps + kEpWarps) {
+    // ---------------- epilogue (warps 16..19, TMEM lane quadrant warp % 4) ----------------
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint32_t ic = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++ic) {
       const Item t = decode_item(a, i);
       const int d = ic & 1;
-      if (!mbar_wait(smem_u32(dfull + d), (ic >> 1) & 1, err)) break;
+      if (!warp_wait(smem_u32(dfull + d), (ic >> 1) & 1, err)) break;
       fence_after_sync();
-      uint32_t v[4][16];
       const int nch = (t.n + 15) >> 4;
+      for (int c0 = 0; c0 < nch; ++c0) {
+        uint32_t v[16];
+        tmem_ld16(tb + lane_base + 64 * d + 16 * c0, v);
+        tmem_wait_ld();
+        if (MODE == 0) {
+          // lanes l < 16: gate row 16q + l; lanes l + 16: the matching up row
+          const int r = 64 * t.mt + 16 * q + (lane & 15);
+          __half* hrow = a.ws.h16 + static_cast<size_t>(t.row0 + 16 * c0) * a.Imax + kpos8(r);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c < nch) tmem_ld16(tb + lane_base + 64 * d + 16 * c, v[c]);
-      tmem_wait_ld();
+          for (int c = 0; c < 16; ++c)
+            if (16 * c0 + c < t.n) {
+              const float g = __uint_as_float(v[c]);
+              const float u = __shfl_down_sync(0xffffffffu, g, 16);
+              if (lane < 16) {
+                const float silu = g / (1.0f + expf(-g));
+                hrow[static_cast<size_t>(c) * a.Imax] = __float2half_rn(silu * u);
+              }
+            }
+        } else {
+          const int m = 128 * t.mt + 32 * q + lane;
+          float* orow = a.ws.obuf + static_cast<size_t>(t.row0 + 16 * c0) * a.H + m;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (16 * c0 + c < t.n) orow[static_cast<size_t>(c) * a.H] = __uint_as_float(v[c]);
+        }
+      }
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(dempty + d));
-      if (MODE == 0) {
-        if (q >= 2) {
-          float* xr = xch + (32 * (q - 2) + lane) * kXchStride;
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < t.n) xr[c] = __uint_as_float(v[c >> 4][c & 15]);
-        }
-        named_sync(1, kEpWarps * 32);
-        if (q < 2) {
-          const int r = 64 * t.mt + 32 * q + lane;
-          const float* xr = xch + (32 * q + lane) * kXchStride;
-          __half* hrow = a.ws.h16 + static_cast<size_t>(t.row0) * a.Imax + kpos8(r);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < t.n) {
-              const float g = __uint_as_float(v[c >> 4][c & 15]);
-              const float u = xr[c];
-              const float silu = g / (1.0f + expf(-g));
-              hrow[static_cast<size_t>(c) * a.Imax] = __float2half_rn(silu * u);
-            }
-        }
-        named_sync(1, kEpWarps * 32);
-      } else {
-        const int m = 128 * t.mt + 32 * q + lane;
-        float* orow = a.ws.obuf + static_cast<size_t>(t.row0) * a.H + m;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < t.n) orow[static_cast<size_t>(c) * a.H] = __uint_as_float(v[c >> 4][c & 15]);
-      }
     }
   }
 
