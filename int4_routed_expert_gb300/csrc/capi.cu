@@ -410,7 +410,10 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
   const Shape& sh = h->sh;
   const Workspace& ws = h->ws;
   cudaError_t e;
-  if (moe::decode_path_ok(sh, T, h->n_sm)) {
+  // one token: the fused single-kernel path; larger batches: the tensor-core
+  // grouped GEMM when the shape fits it, else the small-batch kernels (T <= 4)
+  // or the SIMT general path
+  if (moe::decode_path_ok(sh, T, h->n_sm) && (T == 1 || !h->tc)) {
     moe::PhaseMarker pm{tr.on() ? &Tracer::mark_cb : nullptr, &tr};
     e = moe::launch_decode(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
                            h->n_sm, &h->decode_calls, pm, s);

@@ -255,12 +255,15 @@ down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
   }
 }
 
-// y_t = (acc ? y_t : 0) + (sum_j w_tj * o_(t,j), slot order) + o_shared_t
+// y_t = (acc ? y_t : 0) + (sum_j w_tj * o_(t,j), slot order) + o_shared_t;
+// block (t, c) covers columns [1024 c, 1024 c + 1024) of token t.
 __global__ void __launch_bounds__(256)
 combine_kernel(Shape sh, int T, Workspace ws, float* __restrict__ y, int accumulate) {
   const int t = blockIdx.x;
   const int H = sh.H, k = sh.k, N = T * k;
-  for (int r = threadIdx.x * 4; r < H; r += 256 * 4) {
+  {
+    const int r = blockIdx.y * 1024 + threadIdx.x * 4;
+    if (r >= H) return;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const int p = ws.inv[t * k + j];
@@ -329,7 +332,7 @@ cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T, const Wo
 
 cudaError_t launch_combine(const Shape& sh, int T, const Workspace& ws, float* y,
                            int accumulate, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(sh, T, ws, y, accumulate);
+  combine_kernel<<<dim3(T, (sh.H + 1023) / 1024), 256, 0, s>>>(sh, T, ws, y, accumulate);
   return cudaGetLastError();
 }
 

@@ -154,6 +154,24 @@ select_kernel(const float* __restrict__ logits, const float* __restrict__ bias, 
               topw + static_cast<size_t>(t) * sh.k);
 }
 
+// One warp per token, everything in registers (shapes accepted by
+// fast_select_epl): same ids and weights as select_kernel.
+template <int EPL>
+__global__ void __launch_bounds__(kSelWarps * 32)
+select_regs_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T,
+                   Shape sh, int32_t* __restrict__ ids, float* __restrict__ topw) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + warp;
+  if (t >= T) return;
+  int id;
+  float w;
+  warp_select_logits<EPL>(logits + static_cast<size_t>(t) * sh.E, bias, sh, id, w);
+  if (lane < sh.k) {
+    ids[static_cast<size_t>(t) * sh.k + lane] = id;
+    topw[static_cast<size_t>(t) * sh.k + lane] = w;
+  }
+}
+
 size_t select_smem(const Shape& sh) {
   const int E = sh.E;
   return static_cast<size_t>(kSelWarps) * (2 * E + sh.n_group + (2 * E + 3) / 4 + 1) * 4;
@@ -176,6 +194,21 @@ cudaError_t launch_router_logits(const float* xf, int T, int H, const float* Wr,
 
 cudaError_t launch_select(const float* logits, const float* bias, int T, const Shape& sh,
                           int32_t* ids, float* topw, cudaStream_t s) {
+  const int grid = (T + kSelWarps - 1) / kSelWarps;
+  switch (fast_select_epl(sh)) {
+#define MOE_SEL_CASE(EPL)                                                                     \
+  case EPL:                                                                                   \
+    select_regs_kernel<EPL><<<grid, kSelWarps * 32, 0, s>>>(logits, bias, T, sh, ids, topw); \
+    return cudaGetLastError();
+    MOE_SEL_CASE(1)
+    MOE_SEL_CASE(2)
+    MOE_SEL_CASE(4)
+    MOE_SEL_CASE(8)
+    MOE_SEL_CASE(16)
+#undef MOE_SEL_CASE
+    default:
+      break;
+  }
   const size_t smem = select_smem(sh);
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(

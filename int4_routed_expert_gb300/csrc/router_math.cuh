@@ -217,11 +217,13 @@ __device__ __forceinline__ uint32_t key_code(float f) {
 // expert id on a tie because lane L holds experts L*EPL .. L*EPL+EPL-1.
 // Lanes < k receive (id, w) of slot `lane` in out_id / out_w.
 template <int EPL>
+__device__ __forceinline__ void warp_select_core(const float (&kv)[EPL], const float (&sv)[EPL],
+                                                 const Shape& sh, int& out_id, float& out_w);
+
+template <int EPL>
 __device__ __forceinline__ void warp_select_regs(const float* gkey, const float* gs,
                                                  const Shape& sh, int& out_id, float& out_w) {
   const int lane = threadIdx.x & 31;
-  const int G = sh.E / sh.n_group;
-  const int lpg = G / EPL;
   float kv[EPL], sv[EPL];
 #pragma unroll
   for (int q = 0; q < EPL; q += (EPL >= 4 ? 4 : EPL)) {
@@ -238,6 +240,31 @@ __device__ __forceinline__ void warp_select_regs(const float* gkey, const float*
       }
     }
   }
+  warp_select_core<EPL>(kv, sv, sh, out_id, out_w);
+}
+
+// Same selection from a token's [E] router logits: lane L scores experts
+// L*EPL .. L*EPL+EPL-1 itself (s = sigmoid(logit), key = s + bias).
+template <int EPL>
+__device__ __forceinline__ void warp_select_logits(const float* glog, const float* bias,
+                                                   const Shape& sh, int& out_id, float& out_w) {
+  const int lane = threadIdx.x & 31;
+  float kv[EPL], sv[EPL];
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    const int e = lane * EPL + q;
+    sv[q] = router_sigmoid(glog[e]);
+    kv[q] = __fadd_rn(sv[q], bias[e]);
+  }
+  warp_select_core<EPL>(kv, sv, sh, out_id, out_w);
+}
+
+template <int EPL>
+__device__ __forceinline__ void warp_select_core(const float (&kv)[EPL], const float (&sv)[EPL],
+                                                 const Shape& sh, int& out_id, float& out_w) {
+  const int lane = threadIdx.x & 31;
+  const int G = sh.E / sh.n_group;
+  const int lpg = G / EPL;
   // group score: top two keys of the lane, merged over the lpg lanes
   float a = -INFINITY, b = -INFINITY;
 #pragma unroll

@@ -442,26 +442,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 __global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, Workspace ws) {
   const int N = T * sh.k, H = sh.H;
   const int row = blockIdx.x;
-  if (row == 0 && threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int b = 0; b < sh.E; b += 32) {
-      const int e = b + lane;
-      const int n = e < sh.E ? ws.counts[e] : 0;
-      const int nc = (n + kNMax - 1) / kNMax;
-      int incl = nc;
+  if (row == 0) {
+    // block-wide exclusive scan of the per-expert chunk counts; thread i
+    // handles experts i * ept .. i * ept + ept - 1 (E <= 1024, 256 threads)
+    __shared__ int wsum[8];
+    const int ept = (sh.E + 255) / 256;
+    const int e0 = threadIdx.x * ept;
+    int mine = 0;
+    for (int q = 0; q < ept; ++q)
+      if (e0 + q < sh.E) mine += (ws.counts[e0 + q] + kNMax - 1) / kNMax;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = mine;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
-      }
-      const int pos = carry + incl - nc;
-      const int off = e < sh.E ? ws.offsets[e] : 0;
-      for (int c = 0; c < nc; ++c)
-        ws.chunks[pos + c] = make_int4(off + kNMax * c, min(kNMax, n - kNMax * c), e, 0);
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
     }
-    if (lane == 0) *ws.n_rchunks = carry;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < 8; ++w) {
+      before += w < warp ? wsum[w] : 0;
+      total += wsum[w];
+    }
+    int pos = before + incl - mine;
+    for (int q = 0; q < ept; ++q) {
+      const int e = e0 + q;
+      if (e >= sh.E) break;
+      const int n = ws.counts[e], off = ws.offsets[e];
+      for (int c = 0; c * kNMax < n; ++c)
+        ws.chunks[pos++] = make_int4(off + kNMax * c, min(kNMax, n - kNMax * c), e, 0);
+    }
+    if (threadIdx.x == 0) *ws.n_rchunks = total;
   }
   const int tok = row < N ? ws.perm[row] / sh.k : row - N;
   const float4* src = reinterpret_cast<const float4*>(ws.xf + static_cast<size_t>(tok) * H);
