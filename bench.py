@@ -173,11 +173,6 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
         return (router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh)
                 + n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
                 + 2 * hrows + T * H * 4)
-    if phase == "decode_router_gate_up":
-        return router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh) + hrows
-    if phase == "decode_down_combine":
-        return (n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
-                + hrows + T * H * 4)
     if phase == "gate_up":
         return (n_act + ns) * expert_gate_up_bytes(sh) + T * H * 4 + hrows
     if phase == "down":

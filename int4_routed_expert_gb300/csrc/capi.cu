@@ -1,5 +1,6 @@
 // C ABI of the MoE layer (include/moe.h): validation, workspace, dispatch
-// between the fused small-batch path and the general path, phase tracing.
+// between the fused single-token kernel, the tensor-core grouped GEMM and
+// the SIMT general path, phase tracing.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -85,10 +86,9 @@ Layout layout_for(const moe_config_t* c) {
   const int Imax = c->n_shared ? (c->inter > c->shared_inter ? c->inter : c->shared_inter)
                                : c->inter;
   // row stride of the activation buffer: Imax floats padded to the
-  // swizzled layout of the small-batch kernels (multiple of 1024)
+  // swizzled layout of the single-token kernel (multiple of 1024)
   L.hstride = ((Imax / 32 + 31) / 32) * 1024;
   const size_t N = Tm * k, R = N + Tm;
-  const size_t Ts = Tm < 4 ? Tm : 4;
   // f16 rows and chunk list of the tensor-core path (shapes it takes only)
   const bool tc = c->hidden % 256 == 0 && c->inter % 256 == 0 &&
                   (!c->n_shared || c->shared_inter % 256 == 0);
@@ -105,8 +105,8 @@ Layout layout_for(const moe_config_t* c) {
       4,                     // n_active
       R * L.hstride * 4,     // hbuf
       R * H * 4,             // obuf
-      Ts * E * 4,            // sval
-      Ts * E * 4,            // skey
+      E * 4,                 // sval
+      E * 4,                 // skey
       256,                   // dev_err
       3 * 32 * 4,            // dslot
       256,                   // gbar
@@ -261,10 +261,8 @@ cudaError_t run_route(moe_layer* h, const void* x, moe_dtype_t dt, int T, const 
 }
 
 const char* kPhaseNames[MOE_N_PHASES] = {
-    "prep",       "router_logits", "select",  "plan",
-    "gate_up",    "down",          "combine", "decode_fused",
-    "decode_router_gate_up", "decode_down_combine",
-    "tc_prep",    "tc_gate_up",    "tc_down"};
+    "prep",    "router_logits", "select",  "plan",       "gate_up", "down",
+    "combine", "decode_fused",  "tc_prep", "tc_gate_up", "tc_down"};
 
 void free_trace(moe_layer* h) {
   if (h->trace_ev) {
@@ -410,27 +408,26 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
   const Shape& sh = h->sh;
   const Workspace& ws = h->ws;
   cudaError_t e;
-  // one token: the fused single-kernel path; larger batches: the tensor-core
-  // grouped GEMM when the shape fits it, else the small-batch kernels (T <= 4)
-  // or the SIMT general path
-  if (moe::decode_path_ok(sh, T, h->n_sm) && (T == 1 || !h->tc)) {
+  // one token: the fused single-kernel path when the shape fits it; else the
+  // tensor-core grouped GEMM when the shape fits that, else the SIMT path
+  if (moe::decode_path_ok(sh, T, h->n_sm)) {
     moe::PhaseMarker pm{tr.on() ? &Tracer::mark_cb : nullptr, &tr};
     e = moe::launch_decode(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
                            h->n_sm, &h->decode_calls, pm, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (small-batch path)");
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (single-token path)");
   } else if (h->tc) {
     e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
     if (e == cudaSuccess) {
       e = moe::launch_tc_prep(sh, T, ws, s);
-      tr.mark(10);
+      tr.mark(8);
     }
     if (e == cudaSuccess) {
       e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 0, h->n_sm, s);
-      tr.mark(11);
+      tr.mark(9);
     }
     if (e == cudaSuccess) {
       e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 1, h->n_sm, s);
-      tr.mark(12);
+      tr.mark(10);
     }
     if (e == cudaSuccess) {
       e = moe::launch_combine(sh, T, ws, y, accumulate, s);

@@ -1,20 +1,12 @@
-// Fused small-batch path (T <= 4 tokens, T*k <= 32 entries): shared
-// definitions of its two kernels.
-//
-//   dec_ab  (cooperative, one CTA per SM)  router logits of the CTA's
-//           experts -> grid barrier -> every warp re-derives the selection
-//           and the routing plan in registers -> gate/up rows of the shared
-//           expert (streamed while the router runs) and of the selected
-//           experts -> h = SiLU(g) * u, written pre-scaled and swizzled.
-//   dec_c   (programmatic dependent launch) down-projection rows of every
-//           selected expert and the shared expert, weighted by the gate
-//           weights, summed into y.
+// Shared definitions of the fused single-token kernel (decode_fused.cuh):
+// arguments, the RMSNorm and activation staging helpers, the grid barrier,
+// the in-kernel router (logits in the fixed order, register selection) and
+// the launch helpers.
 //
 // "GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri hierarchy", N1
 // (MoE bullet), N2 (packed int4 gate/up/down with grouped scales), N4 (route
-// the batch first, stream the union of the selected experts once);
-// "colibri-strix/README.md", "What's implemented" (noaux_tc router, shared
-// expert, batch-union MoE).
+// first, stream the selected experts once); "colibri-strix/README.md",
+// "What's implemented" (noaux_tc router, shared expert).
 #pragma once
 
 #include "moe_internal.cuh"
@@ -25,7 +17,6 @@ namespace moe {
 namespace dec {
 
 constexpr int kMaxEntries = 32;       // T * k
-constexpr int kMaxNT = 4;             // tokens per call
 constexpr int kRowsC = 4;             // down-projection rows per item
 constexpr int kMaxLocalExperts = 8;   // router experts per CTA
 constexpr int kRouterWarps = 8;       // one warp per logit segment
@@ -153,123 +144,10 @@ __device__ inline bool gbar_wait(unsigned long long* p, unsigned long long targe
   return ok != 0;
 }
 
-// The routing plan of the call, one selected expert ("slot") per lane.
-struct LanePlan {
-  int n_act;       // slots (distinct experts), warp-uniform
-  int e;           // expert of slot `lane` (lane < n_act)
-  int p0;          // first plan position of the slot
-  int n;           // entries of the slot
-  unsigned tmask;  // tokens of the slot (bit t)
-  float w;         // gate weight of the slot's first entry
-};
-
 template <int EPL>
 __device__ __forceinline__ void select_token(const DecArgs& a, int t, int& id, float& w) {
   const size_t o = static_cast<size_t>(t) * a.sh.E;
   warp_select_regs<EPL>(a.ws.skey + o, a.ws.sval + o, a.sh, id, w);
-}
-
-// Every warp derives the selection of the call's T tokens from the
-// published scores (bit-identical in every warp), then the plan: entries
-// i = t*k + j grouped by expert ascending, ascending i inside an expert.
-// With `publish`, the plan is also written to the workspace.
-__device__ __forceinline__ void warp_route_plan_inl(const DecArgs& a, int epl, bool publish,
-                                                   LanePlan& lp) {
-  const int lane = threadIdx.x & 31;
-  const int k = a.sh.k, T = a.T, N = T * k;
-  int my_id = 0;
-  float my_w = 0.0f;
-  for (int t = 0; t < T; ++t) {
-    int id;
-    float w;
-    switch (epl) {
-      case 1: select_token<1>(a, t, id, w); break;
-      case 2: select_token<2>(a, t, id, w); break;
-      case 4: select_token<4>(a, t, id, w); break;
-      default: select_token<8>(a, t, id, w); break;
-    }
-    const int src = lane - t * k;
-    const int sid = __shfl_sync(0xffffffffu, id, src & 31);
-    const float sw = __shfl_sync(0xffffffffu, w, src & 31);
-    if (src >= 0 && src < k) {
-      my_id = sid;
-      my_w = sw;
-    }
-  }
-  const bool valid = lane < N;
-  const int e = valid ? my_id : 0x40000000 + lane;  // distinct dummies
-  const unsigned lt = (1u << lane) - 1u;
-  const unsigned grp = __match_any_sync(0xffffffffu, e);
-  const int rank = __popc(grp & lt), cnt = __popc(grp);
-  const bool leader = valid && (grp & lt) == 0;
-  const unsigned leaders = __ballot_sync(0xffffffffu, leader);
-  int before = 0, base = 0;
-  for (unsigned m = leaders; m; m &= m - 1) {
-    const int l = __ffs(m) - 1;
-    const int el = __shfl_sync(0xffffffffu, e, l);
-    const int cl = __shfl_sync(0xffffffffu, cnt, l);
-    if (el < e) {
-      ++before;
-      base += cl;
-    }
-  }
-  unsigned tmask = 0;
-  for (unsigned m = grp; m; m &= m - 1) tmask |= 1u << ((__ffs(m) - 1) / k);
-  lp.n_act = __popc(leaders);
-  lp.e = 0;
-  lp.p0 = 0;
-  lp.n = 0;
-  lp.tmask = 0;
-  lp.w = 0.0f;
-  for (unsigned m = leaders; m; m &= m - 1) {
-    const int l = __ffs(m) - 1;
-    const int al = __shfl_sync(0xffffffffu, before, l);
-    const int el = __shfl_sync(0xffffffffu, e, l);
-    const int bl = __shfl_sync(0xffffffffu, base, l);
-    const int cl = __shfl_sync(0xffffffffu, cnt, l);
-    const unsigned tl = __shfl_sync(0xffffffffu, tmask, l);
-    const float wl = __shfl_sync(0xffffffffu, my_w, l);
-    if (lane == al) {
-      lp.e = el;
-      lp.p0 = bl;
-      lp.n = cl;
-      lp.tmask = tl;
-      lp.w = wl;
-    }
-  }
-  if (publish) {
-    const Workspace& ws = a.ws;
-    if (valid) {
-      const int p = base + rank;
-      ws.ids[lane] = my_id;
-      ws.topw[lane] = my_w;
-      ws.perm[p] = lane;
-      ws.inv[lane] = p;
-    }
-    if (lane < lp.n_act) {
-      ws.active[lane] = lp.e;
-      ws.dslot[lane] = lp.e;
-      ws.dslot[32 + lane] = lp.p0;
-      ws.dslot[64 + lane] = lp.n;
-    }
-    if (lane == 0) *ws.n_active = lp.n_act;
-    // per-expert counts and exclusive offsets over all E experts
-    for (int e0 = 0; e0 < a.sh.E; e0 += 32) {
-      const int ex = e0 + lane;
-      int c = 0, off = 0;
-      for (int q = 0; q < lp.n_act; ++q) {
-        const int eq = __shfl_sync(0xffffffffu, lp.e, q);
-        const int nq = __shfl_sync(0xffffffffu, lp.n, q);
-        if (eq == ex) c = nq;
-        if (eq < ex) off += nq;
-      }
-      if (ex < a.sh.E) {
-        ws.counts[ex] = c;
-        ws.offsets[ex] = off;
-      }
-    }
-    if (lane == 0) ws.offsets[a.sh.E] = N;
-  }
 }
 
 // Router logits from shared memory: xn = x_hat in natural order [H], wr =
@@ -313,12 +191,6 @@ __device__ __forceinline__ void router_cta_smem(const DecArgs& a, const float* x
       a.ws.skey[e] = __fadd_rn(sv, __ldg(a.w.router_bias + e));
     }
   }
-}
-
-// Out-of-line copy for kernels with many instantiations.
-static __device__ __noinline__ void warp_route_plan(const DecArgs& a, int epl, bool publish,
-                                                    LanePlan& lp) {
-  warp_route_plan_inl(a, epl, publish, lp);
 }
 
 // Router logits of this CTA's experts (blockIdx.x + l * gridDim.x) by warps
@@ -432,45 +304,6 @@ cudaError_t set_smem_once(K kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
 }
-
-// Configurations of the two kernels (the .cu files instantiate these).
-constexpr int kStagesB1 = 2, kWarpsB1 = 12;  // dec_ab, one token
-constexpr int kStagesB4 = 2, kWarpsB4 = 8;   // dec_ab, up to four tokens
-constexpr int kStagesC = 3, kWarpsC = 8;     // dec_c
-
-// Bytes of dynamic shared memory of dec_ab for a shape and NT.
-__host__ __device__ inline size_t ab_smem_bytes(const Shape& sh, int NT, int warps, int stages,
-                                                int n_sm) {
-  const int L = (sh.E + n_sm - 1) / n_sm;
-  size_t b = static_cast<size_t>(NT) * swz_pad(sh.H) * 4;              // xs
-  b += static_cast<size_t>(warps) * stages * (sh.H + sh.H / 8);        // rings
-  b += static_cast<size_t>(warps) * stages * 8;                        // mbarriers
-  b += static_cast<size_t>(L) * kRouterWarps * NT * 4;                 // logit segments
-  b += 8 * 8 + 16;                                                     // fp64 partials, rf
-  return b;
-}
-
-__host__ __device__ inline size_t c_ring_bytes(const Shape& sh, int warps, int stages) {
-  return static_cast<size_t>(warps) * stages * kRowsC * (sh.I / 2 + sh.I / 16);
-}
-
-__host__ __device__ inline size_t c_h_bytes(const Shape& sh, int T, int hstride) {
-  return static_cast<size_t>(T * sh.k + T) * hstride * 4;
-}
-
-__host__ __device__ inline size_t c_smem_bytes(const Shape& sh, int T, int NT, bool h_smem,
-                                               int hstride) {
-  size_t b = c_ring_bytes(sh, kWarpsC, kStagesC);
-  b += static_cast<size_t>(kWarpsC) * kStagesC * 8 + 16;             // mbarriers (+h barrier)
-  b += static_cast<size_t>(kWarpsC) * 2 * kRowsC * NT * 4;           // partial rows
-  if (h_smem) b += c_h_bytes(sh, T, hstride);
-  return b;
-}
-
-cudaError_t launch_dec_ab(const DecArgs& a, int NT, int cpl, size_t smem, int n_sm,
-                          cudaStream_t s);
-cudaError_t launch_dec_c(const DecArgs& a, int NT, int cpl, bool h_smem, size_t smem, int n_sm,
-                         bool pdl, cudaStream_t s);
 
 }  // namespace dec
 }  // namespace moe

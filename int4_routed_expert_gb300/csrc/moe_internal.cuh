@@ -24,11 +24,11 @@ struct Workspace {
   int32_t* n_active; // [1]
   float* hbuf;       // [Tm*k + Tm][hstride] SwiGLU activations (routed, then shared)
   float* obuf;       // [Tm*k + Tm][H]       expert outputs before the combine
-  float* sval;       // [Tm][E] un-biased router scores (small-batch path)
-  float* skey;       // [Tm][E] selection keys s + bias (small-batch path)
+  float* sval;       // [E] un-biased router scores (single-token kernel)
+  float* skey;       // [E] selection keys s + bias (single-token kernel)
   int32_t* dev_err;  // device error word (bounded waits that gave up)
-  int32_t* dslot;    // [3][32] small-batch slot table: expert, first position, entries
-  unsigned long long* gbar;  // grid barrier counter of the small-batch kernel (monotonic)
+  int32_t* dslot;    // [3][32] single-token slot table: expert, first position, entries
+  unsigned long long* gbar;  // grid barrier counter of the single-token kernel (monotonic)
   __half* x16;       // [Tm*k + Tm][H]    f16 activation rows of the tensor-core path
   __half* h16;       // [Tm*k + Tm][Imax] f16 SwiGLU rows of the tensor-core path
   int4* chunks;      // routed chunks of <= 64 plan rows: {first row, rows, expert, 0}
@@ -44,7 +44,7 @@ struct Shape {
 }  // namespace moe
 
 // Phase ids of the trace API (a call records only the phases it runs).
-#define MOE_N_PHASES 13
+#define MOE_N_PHASES 11
 
 namespace moe {
 struct TcMaps;  // TMA tensor maps of the tensor-core grouped GEMM (tc_gemm.cu)
@@ -60,7 +60,7 @@ struct moe_layer {
   int device;
   char err[512];
   int n_sm;
-  unsigned long long decode_calls;  // small-batch launches so far (grid barrier targets)
+  unsigned long long decode_calls;  // single-token barrier rounds so far (grid barrier targets)
   moe::TcMaps* tc;                  // NULL when the shape does not fit the tensor-core path
   // phase tracing: trace_cap calls x (MOE_N_PHASES + 1) events, and per call
   // the phase id recorded after each launched phase
@@ -120,9 +120,8 @@ cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStre
 cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Workspace& ws, int mode,
                            int n_sm, cudaStream_t s);
 
-// Fused small-batch path (T <= 4, T*k <= 32).  When `marker.fn` is set
-// (phase tracing), the kernels are launched without the programmatic-
-// dependency overlap and marker.fn(ctx, phase) is called after each of them.
+// Fused single-token kernel.  When `marker.fn` is set (phase tracing),
+// marker.fn(ctx, phase) is called after the launch.
 struct PhaseMarker {
   void (*fn)(void* ctx, int phase);
   void* ctx;
@@ -131,7 +130,7 @@ struct PhaseMarker {
   }
 };
 bool decode_path_ok(const Shape& sh, int T, int n_sm);
-// calls: the handle's count of small-batch launches (read and advanced).
+// calls: the handle's count of grid-barrier rounds (read and advanced).
 cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const void* x,
                           moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,
                           float* y, int accumulate, int n_sm, unsigned long long* calls,

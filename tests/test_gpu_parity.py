@@ -89,7 +89,8 @@ def test_tiny_layer(m, T):
 
 SHAPES = [
     # H, I, E, k, n_group, topk_group, n_shared  (I % 256 == 0 and E <= 256 with
-    # E = 32 * 2^j take the fused small-batch path for T <= 4)
+    # E = 32 * 2^j take the fused single-token kernel for T = 1; T > 1 with
+    # I % 256 == 0 takes the grouped GEMM)
     (256, 256, 32, 4, 4, 2, 1),
     (512, 512, 64, 6, 8, 3, 1),
     (1024, 256, 128, 8, 8, 4, 1),
@@ -230,7 +231,7 @@ def test_trace_phases(m):
     h.forward(gen_activations(wl, 20, call=1).to(DEV))
     h.forward(gen_activations(wl, 3, call=2).to(DEV))
     names, rows = m.moe_trace_read(h.h, 3)
-    assert len(rows) == 3 and len(names) == 13
+    assert len(rows) == 3 and len(names) == 11
     small = {n for n, v in zip(names, rows[0]) if v > 0}
     tc = {n for n, v in zip(names, rows[1]) if v > 0}
     assert small == {"decode_fused"}
@@ -271,6 +272,21 @@ def test_tc_grouped_gemm(m, shape, T):
     L = gen_layer(wl, device=DEV)
     x = gen_activations(wl, T, call=0)
     _run_full(m, wl, L, x, max_tokens=T + 3)
+
+
+def test_single_token_wide_intermediate(m):
+    """One token with an intermediate size the fused single-token kernel
+    does not keep in registers (I = 4096): the grouped GEMM takes it."""
+    sh = LayerShape(512, 4096, 32, 4, 4, 2, 2.5)
+    wl = Workload("tc_t1", sh, 1, 1, "bf16", "zipf", 7803)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 2)
+    m.moe_trace_enable(h.h, 1)
+    _run_full(m, wl, L, gen_activations(wl, 1, call=0), handle=h)
+    names, rows = m.moe_trace_read(h.h, 1)
+    assert "tc_gate_up" in {n for n, v in zip(names, rows[0]) if v > 0}
+    m.moe_trace_enable(h.h, 0)
+    h.close()
 
 
 def test_tc_multi_chunk_experts(m):
