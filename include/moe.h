@@ -186,7 +186,7 @@ size_t moe_workspace_bytes(const moe_config_t* cfg);
  * traced call c to ms[c * n_phases + p] for c < min(cap, traced calls)
  * (0 for phases the call did not run), stores the counts, and restarts the
  * trace for the next n calls.  ms must hold cap * n_phases floats, with
- * n_phases = 11 (the phase ids of moe_trace_phase_name).
+ * n_phases = 12 (the phase ids of moe_trace_phase_name).
  * moe_trace_phase_name(p): static name of phase p (NULL when out of range).
  * Tracing is off by default. */
 moe_status_t moe_trace_enable(moe_layer_t* h, int n_calls);

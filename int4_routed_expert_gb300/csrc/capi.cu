@@ -89,6 +89,7 @@ Layout layout_for(const moe_config_t* c) {
   // swizzled layout of the single-token kernel (multiple of 1024)
   L.hstride = ((Imax / 32 + 31) / 32) * 1024;
   const size_t N = Tm * k, R = N + Tm;
+  const size_t Ts = Tm < 4 ? Tm : 4;  // tokens of the in-kernel routers
   // f16 rows and chunk list of the tensor-core path (shapes it takes only)
   const bool tc = c->hidden % 256 == 0 && c->inter % 256 == 0 &&
                   (!c->n_shared || c->shared_inter % 256 == 0);
@@ -105,8 +106,8 @@ Layout layout_for(const moe_config_t* c) {
       4,                     // n_active
       R * L.hstride * 4,     // hbuf
       R * H * 4,             // obuf
-      E * 4,                 // sval
-      E * 4,                 // skey
+      Ts * E * 4,            // sval
+      Ts * E * 4,            // skey
       256,                   // dev_err
       3 * 32 * 4,            // dslot
       256,                   // gbar
@@ -262,7 +263,7 @@ cudaError_t run_route(moe_layer* h, const void* x, moe_dtype_t dt, int T, const 
 
 const char* kPhaseNames[MOE_N_PHASES] = {
     "prep",    "router_logits", "select",  "plan",       "gate_up", "down",
-    "combine", "decode_fused",  "tc_prep", "tc_gate_up", "tc_down"};
+    "combine", "decode_fused",  "tc_prep", "tc_gate_up", "tc_down", "tc_front"};
 
 void free_trace(moe_layer* h) {
   if (h->trace_ev) {
@@ -416,24 +417,28 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
                            h->n_sm, &h->decode_calls, pm, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (single-token path)");
   } else if (h->tc) {
-    e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
-    if (e == cudaSuccess) {
+    if (moe::front_path_ok(sh, T, h->n_sm)) {
+      // small batch: routing, plan and f16 rows in one cooperative kernel
+      e = moe::launch_front(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, h->n_sm,
+                            &h->decode_calls, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (routing front end)");
+      tr.mark(11);
+    } else {
+      e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
+      if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (routing)");
       e = moe::launch_tc_prep(sh, T, ws, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (grouped GEMM rows)");
       tr.mark(8);
     }
-    if (e == cudaSuccess) {
-      e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 0, h->n_sm, s);
-      tr.mark(9);
-    }
-    if (e == cudaSuccess) {
-      e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 1, h->n_sm, s);
-      tr.mark(10);
-    }
-    if (e == cudaSuccess) {
-      e = moe::launch_combine(sh, T, ws, y, accumulate, s);
-      tr.mark(6);
-    }
-    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (tensor-core path)");
+    e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 0, h->n_sm, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (grouped GEMM gate/up)");
+    tr.mark(9);
+    e = moe::launch_tc_gemm(*h->tc, sh, T, ws, 1, h->n_sm, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (grouped GEMM down)");
+    tr.mark(10);
+    e = moe::launch_combine(sh, T, ws, y, accumulate, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (combine)");
+    tr.mark(6);
   } else {
     e = run_route(h, x, dtype, T, rms_gamma, rms_eps, s, tr);
     if (e == cudaSuccess) {

@@ -24,8 +24,8 @@ struct Workspace {
   int32_t* n_active; // [1]
   float* hbuf;       // [Tm*k + Tm][hstride] SwiGLU activations (routed, then shared)
   float* obuf;       // [Tm*k + Tm][H]       expert outputs before the combine
-  float* sval;       // [E] un-biased router scores (single-token kernel)
-  float* skey;       // [E] selection keys s + bias (single-token kernel)
+  float* sval;       // [min(Tm,4)][E] un-biased router scores (in-kernel routers)
+  float* skey;       // [min(Tm,4)][E] selection keys s + bias (in-kernel routers)
   int32_t* dev_err;  // device error word (bounded waits that gave up)
   int32_t* dslot;    // [3][32] single-token slot table: expert, first position, entries
   unsigned long long* gbar;  // grid barrier counter of the single-token kernel (monotonic)
@@ -44,7 +44,7 @@ struct Shape {
 }  // namespace moe
 
 // Phase ids of the trace API (a call records only the phases it runs).
-#define MOE_N_PHASES 11
+#define MOE_N_PHASES 12
 
 namespace moe {
 struct TcMaps;  // TMA tensor maps of the tensor-core grouped GEMM (tc_gemm.cu)
@@ -119,6 +119,14 @@ cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStre
 // mode 0: gate/up -> h16; mode 1: down -> obuf
 cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Workspace& ws, int mode,
                            int n_sm, cudaStream_t s);
+
+// Small-batch routing front end of the grouped GEMM (front.cu): prep,
+// logits, selection, plan, chunk list and f16 rows in one cooperative
+// kernel for T <= 4.  calls: as for launch_decode.
+bool front_path_ok(const Shape& sh, int T, int n_sm);
+cudaError_t launch_front(const moe_weights_t& w, const Shape& sh, int T, const void* x,
+                         moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,
+                         int n_sm, unsigned long long* calls, cudaStream_t s);
 
 // Fused single-token kernel.  When `marker.fn` is set (phase tracing),
 // marker.fn(ctx, phase) is called after the launch.

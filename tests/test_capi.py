@@ -112,10 +112,10 @@ def test_null_handle(m):
 
 
 def test_phase_names(m):
-    names = [m.moe_trace_phase_name(p) for p in range(11)]
-    assert all(names) and len(set(names)) == 11
+    names = [m.moe_trace_phase_name(p) for p in range(12)]
+    assert all(names) and len(set(names)) == 12
     assert {"tc_prep", "tc_gate_up", "tc_down"} <= set(names)
-    assert m.moe_trace_phase_name(11) is None and m.moe_trace_phase_name(-1) is None
+    assert m.moe_trace_phase_name(12) is None and m.moe_trace_phase_name(-1) is None
 
 
 def test_binding_does_not_touch_the_oracle():
