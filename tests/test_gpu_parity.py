@@ -265,8 +265,11 @@ TC_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("T", [5, 40, 150])
+@pytest.mark.parametrize("T", [3, 5, 40, 150])
 def test_tc_grouped_gemm(m, shape, T):
+    """T = 3 takes the small-batch routing front end where the shape allows
+    (32 experts: 768 x 256 with a 512-wide shared expert), the five routing
+    kernels otherwise."""
     H, I, E, k, ng, tg, ns, Is = shape
     sh = LayerShape(H, I, E, k, ng, tg, 2.5, n_shared=ns, shared_inter=Is)
     wl = Workload("tc", sh, T, 1, "bf16" if T % 2 else "f32", "zipf", 7700 + H + I + E + T)
