@@ -116,6 +116,15 @@ __device__ __forceinline__ Item decode_item(const Args& a, int i) {
   return t;
 }
 
+// Item i, or an empty item past the end.  The roles decode the next item one
+// item ahead, so that the chunk-list load is off the item boundary.
+__device__ __forceinline__ Item item_or_empty(const Args& a, int i, int total) {
+  if (i < total) return decode_item(a, i);
+  Item t;
+  t.row0 = t.n = t.e = t.mt = 0;
+  return t;
+}
+
 __device__ __forceinline__ uint32_t lop(uint32_t v, uint32_t mask) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(0x64006400u));
@@ -236,8 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint64_t pol = policy_evict_first();  // weights are read once
     uint32_t it = 0;
     bool failed = false;
+    Item tn = item_or_empty(a, blockIdx.x, total);
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
-      const Item t = decode_item(a, i);
+      const Item t = tn;
+      tn = item_or_empty(a, i + gridDim.x, total);
       const int sh = t.e < 0 ? 1 : 0;
       const int KS = sh ? a.ks_s : a.ks_r;
       const int ya = MODE == 0 ? (sh ? 0 : t.e * a.I) + 64 * t.mt
@@ -277,8 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint64_t pol = policy_evict_last();  // activation rows are re-read by other CTAs
     uint32_t it = 0;
     bool failed = false;
+    Item tn = item_or_empty(a, blockIdx.x, total);
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
-      const Item t = decode_item(a, i);
+      const Item t = tn;
+      tn = item_or_empty(a, i + gridDim.x, total);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       const int nb = (t.n + 15) >> 4;
       for (int ks = 0; ks < KS; ++ks, ++it) {
@@ -306,8 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ---------------- MMA issuer ----------------
     uint32_t it = 0, ic = 0;
     bool failed = false;
+    Item tn = item_or_empty(a, blockIdx.x, total);
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x, ++ic) {
-      const Item t = decode_item(a, i);
+      const Item t = tn;
+      tn = item_or_empty(a, i + gridDim.x, total);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       const uint32_t idesc = idesc_f16(128, ((t.n + 15) >> 4) * 16);
       const int d = ic & 1;
@@ -346,8 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint32_t it = 0;
     bool failed = false;
+    Item tn = item_or_empty(a, blockIdx.x, total);
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
-      const Item t = decode_item(a, i);
+      const Item t = tn;
+      tn = item_or_empty(a, i + gridDim.x, total);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int s = it % kWStages, ab = it % kABufs;
@@ -390,8 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint32_t ic = 0;
+    Item tn = item_or_empty(a, blockIdx.x, total);
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++ic) {
-      const Item t = decode_item(a, i);
+      const Item t = tn;
+      tn = item_or_empty(a, i + gridDim.x, total);
       const int d = ic & 1;
       if (!warp_wait(smem_u32(dfull + d), (ic >> 1) & 1, err)) break;
       fence_after_sync();
