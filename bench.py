@@ -129,6 +129,28 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (burst: the kernel is timed alone); f16 runs at the
+    same rate on the tensor cores."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def phase_flops(phase, sh, T):
+    """Tensor-core flops of one launch of a grouped-GEMM phase: 2 per
+    multiply-add over every plan row and shared-expert row."""
+    rows = T * sh.top_k
+    srows = T if sh.n_shared else 0
+    if phase == "tc_gate_up":
+        return 2 * 2 * sh.hidden * (rows * sh.inter + srows * sh.i_shared)
+    if phase == "tc_down":
+        return 2 * sh.hidden * (rows * sh.inter + srows * sh.i_shared)
+    return None
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int4_routed_expert_gb300", "csrc")
@@ -419,7 +441,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="glm_decode",
-                    choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack"])
+                    choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
+                             "glm_prefill_uniform"])
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
     ap.add_argument("--calls", type=int, default=None, help="override calls per step")
     ap.add_argument("--layers", type=int, default=None, help="override stacked layers")
@@ -518,6 +541,29 @@ def main():
 
     if rank == 0:
         achieved = kb / (per_launch_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": dominant,
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                    "traffic": ncu_traffic(dominant, workload_key(wl, args.experts, args.tokens)),
+                    "algorithmic_bytes_per_launch": kb,
+                    "avg_launch_us": round(1000 * per_launch_ms, 3),
+                    "duration_source": "CUDA events between the kernels in a traced pass "
+                                       "of the same step right after the timed region"}
+        fl = phase_flops(dominant, sh, T)
+        if wl.extra.get("bound") == "tensor" and fl:
+            tpeak, tkind = measured_tensor_peak()
+            tach = fl / (per_launch_ms / 1000.0) / 1e12
+            roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(tach, 1),
+                        "peak": tpeak, "unit": "TFLOP/s", "frac": round(tach / tpeak, 4),
+                        "peak_kind": tkind, "traffic": roofline["traffic"],
+                        "algorithmic_flops_per_launch": fl,
+                        "avg_launch_us": roofline["avg_launch_us"],
+                        "duration_source": roofline["duration_source"],
+                        "hbm": {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}}
+        for name in kernels:
+            f = phase_flops(name, sh, T)
+            if f:
+                kernels[name]["tflops"] = round(f / (kernels[name]["avg_us"] / 1e6) / 1e12, 1)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -534,14 +580,7 @@ def main():
                 "unflushed_tokens_per_s": round(tokens_step / (unflushed_ms / 1000.0), 1),
                 "parallelism": f"replicas x{world}",
             },
-            "roofline": {"bound": "hbm", "kernel": dominant,
-                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "traffic": ncu_traffic(dominant, workload_key(wl, args.experts, args.tokens)),
-                         "algorithmic_bytes_per_launch": kb,
-                         "avg_launch_us": round(1000 * per_launch_ms, 3),
-                         "duration_source": "CUDA events between the kernels in a traced pass "
-                                            "of the same step right after the timed region"},
+            "roofline": roofline,
             "layer_hbm": {"bytes_per_call": layer_bytes, "gbs": round(layer_gbs, 1),
                           "pct_of_8tbs": round(100 * layer_gbs / NOMINAL_HBM_GBS, 1),
                           "frac_of_measured": round(layer_gbs / peak, 4),

@@ -63,22 +63,35 @@ struct TcMaps {
 
 namespace tc {
 
-constexpr int kWStages = 7;                  // weight-tile ring depth
-constexpr int kBStages = 3;                  // activation-row ring depth
 constexpr int kKS = 256;                     // K per stage
-constexpr int kNMax = 64;                    // tokens per chunk
 constexpr int kAQBytes = 128 * 128;          // int4 tile: 128 rows x 256 nibbles
 constexpr int kASBytes = 128 * 16;           // 8 f16 scales per row
 constexpr int kWBytes = kAQBytes + kASBytes; // 18432, multiple of 1024
-constexpr int kSlabBytes = kNMax * 128;      // 64 rows x 64 f16
-constexpr int kBBytes = 4 * kSlabBytes;      // 32768
 constexpr int kDqWarps = 16, kEpWarps = 4;
 constexpr int kWarpWProd = kDqWarps + kEpWarps, kWarpBProd = kWarpWProd + 1,
               kWarpMma = kWarpBProd + 1;
 constexpr int kThreads = (kWarpMma + 1) * 32;  // 736
-constexpr int kABufs = kBStages;  // A buffers and B slots advance together
-constexpr uint32_t kTmemCols = 512;  // D: 2 x 64 columns, A: 3 x 128 columns
-constexpr int kSmemBytes = 1024 + kBStages * kBBytes + kWStages * kWBytes + 512;
+constexpr uint32_t kTmemCols = 512;
+
+// Two instantiations by the rows of a chunk (the MMA's N):
+//   NMAX = 64:  7-deep weight ring, 3 activation slots of 32 KB, 3 TMEM A
+//               buffers, two 64-column accumulators (batches of a few rows
+//               per expert: the weight stream is the bound)
+//   NMAX = 128: 5-deep weight ring, 2 activation slots of 64 KB, 2 A buffers,
+//               two 128-column accumulators (many rows per expert: an
+//               M = 128, N = 128 MMA runs the tensor core at full rate)
+// TMEM columns: accumulator d at NMAX * d, A buffer b at 2 * NMAX + 128 * b.
+template <int NMAX>
+struct Cfg {
+  static constexpr int kNMax = NMAX;
+  static constexpr int kBStages = NMAX == 64 ? 3 : 2;
+  static constexpr int kABufs = kBStages;  // A buffers and B slots advance together
+  static constexpr int kWStages = NMAX == 64 ? 7 : 5;
+  static constexpr int kSlabBytes = NMAX * 128;  // NMAX rows x 64 f16
+  static constexpr int kBBytes = 4 * kSlabBytes;
+  static constexpr int kSmemBytes = 1024 + kBStages * kBBytes + kWStages * kWBytes + 512;
+  static_assert(2 * NMAX + 128 * kABufs <= static_cast<int>(kTmemCols), "TMEM columns");
+};
 
 struct Args {
   CUtensorMap aq[2][2];  // [routed, shared][gate, up] (down: [..][0])
@@ -89,6 +102,7 @@ struct Args {
   int mt_r, mt_s;    // M tiles per chunk (routed, shared)
   int ks_r, ks_s;    // K stages per item
   int n_sh_chunks;
+  int chunk;         // rows per chunk (the instantiation's NMAX)
 };
 
 struct Item {
@@ -101,8 +115,8 @@ __device__ __forceinline__ Item decode_item(const Args& a, int i) {
   if (i < n_sh_items) {
     const int c = i / a.mt_s;
     t.mt = i - c * a.mt_s;
-    t.row0 = a.N + kNMax * c;
-    t.n = min(kNMax, a.T - kNMax * c);
+    t.row0 = a.N + a.chunk * c;
+    t.n = min(a.chunk, a.T - a.chunk * c);
     t.e = -1;
   } else {
     const int j = i - n_sh_items;
@@ -187,8 +201,11 @@ __device__ __forceinline__ int tile_row(int L) {
   return l < 16 ? 16 * q + l : 48 + 16 * q + l;
 }
 
-template <int MODE>  // 0: gate/up, 1: down
+template <int MODE, int NMAX>  // MODE 0: gate/up, 1: down
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Args a) {
+  using C = Cfg<NMAX>;
+  constexpr int kWStages = C::kWStages, kBStages = C::kBStages, kABufs = C::kABufs;
+  constexpr int kSlabBytes = C::kSlabBytes, kBBytes = C::kBBytes;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const int d = ic & 1;
       if (!warp_wait(smem_u32(dempty + d), ((ic >> 1) & 1) ^ 1, err)) break;
       fence_after_sync();
-      const uint32_t dt = tb + 64 * d;
+      const uint32_t dt = tb + NMAX * d;
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int sb = it % kBStages;  // B slot, A buffer and done barrier share the index
         if (!warp_wait(smem_u32(bfull + sb), (it / kBStages) & 1, err) ||
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         fence_after_sync();
-        const uint32_t at = tb + 128 + 128 * sb;
+        const uint32_t at = tb + 2 * NMAX + 128 * sb;
         // descriptor of slab 0; later slabs / K steps add (byte offset >> 4) to the
         // 14-bit start field, which stays below 2^14 inside shared memory
         const uint64_t bd = sdesc_sw128(smem_u32(bring + sb * kBBytes));
@@ -395,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         dq_word_f16(w1.y, s1, v + 20);
         dq_word_f16(w1.z, s1, v + 24);
         dq_word_f16(w1.w, s1, v + 28);
-        tmem_st32(tb + lane_base + 128 + 128 * ab + 32 * j, v);
+        tmem_st32(tb + lane_base + 2 * NMAX + 128 * ab + 32 * j, v);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
@@ -417,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const int nch = (t.n + 15) >> 4;
       for (int c0 = 0; c0 < nch; ++c0) {
         uint32_t v[16];
-        tmem_ld16(tb + lane_base + 64 * d + 16 * c0, v);
+        tmem_ld16(tb + lane_base + NMAX * d + 16 * c0, v);
         tmem_wait_ld();
         if (MODE == 0) {
           // lanes l < 16: gate row 16q + l; lanes l + 16: the matching up row
@@ -458,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 // Routed chunk list (warp 0 of block 0) and the f16 activation rows: row p <
 // T*k holds token perm[p] / k, row T*k + t token t, each in the 8-element
 // order of the dequantised weights.
-__global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, Workspace ws) {
+__global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, int cr, Workspace ws) {
   const int N = T * sh.k, H = sh.H;
   const int row = blockIdx.x;
   if (row == 0) {
@@ -469,7 +486,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, Workspace
     const int e0 = threadIdx.x * ept;
     int mine = 0;
     for (int q = 0; q < ept; ++q)
-      if (e0 + q < sh.E) mine += (ws.counts[e0 + q] + kNMax - 1) / kNMax;
+      if (e0 + q < sh.E) mine += (ws.counts[e0 + q] + cr - 1) / cr;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = mine;
 #pragma unroll
@@ -489,8 +506,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(Shape sh, int T, Workspace
       const int e = e0 + q;
       if (e >= sh.E) break;
       const int n = ws.counts[e], off = ws.offsets[e];
-      for (int c = 0; c * kNMax < n; ++c)
-        ws.chunks[pos++] = make_int4(off + kNMax * c, min(kNMax, n - kNMax * c), e, 0);
+      for (int c = 0; c * cr < n; ++c)
+        ws.chunks[pos++] = make_int4(off + cr * c, min(cr, n - cr * c), e, 0);
     }
     if (threadIdx.x == 0) *ws.n_rchunks = total;
   }
@@ -559,7 +576,7 @@ bool tc_path_ok(const Shape& sh) {
 }
 
 size_t tc_max_chunks(int Tm, int k, int E) {
-  return static_cast<size_t>(Tm) * k / tc::kNMax + E + 1;
+  return static_cast<size_t>(Tm) * k / 64 + E + 1;  // chunks of >= 64 rows
 }
 
 TcMaps* tc_create_maps(const moe_weights_t& w, const Shape& sh, const Workspace& ws, int Tm) {
@@ -598,11 +615,35 @@ TcMaps* tc_create_maps(const moe_weights_t& w, const Shape& sh, const Workspace&
 
 void tc_destroy_maps(TcMaps* m) { delete m; }
 
+// Rows per chunk for a batch: 128 when the experts average at least 64 plan
+// rows (the tensor core then runs full-width MMAs), else 64.
+int tc_chunk_rows(const Shape& sh, int T) {
+  return static_cast<long long>(T) * sh.k >= 64LL * sh.E ? 128 : 64;
+}
+
 cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStream_t s) {
   const int rows = T * sh.k + (sh.n_shared ? T : 0);
-  tc::tc_prep_kernel<<<rows, 256, 0, s>>>(sh, T, ws);
+  tc::tc_prep_kernel<<<rows, 256, 0, s>>>(sh, T, tc_chunk_rows(sh, T), ws);
   return cudaGetLastError();
 }
+
+namespace tc {
+namespace {
+template <int MODE, int NMAX>
+cudaError_t launch_gemm_inst(const Args& a, int n_sm, cudaStream_t s) {
+  static bool attr_set = false;
+  constexpr int smem = Cfg<NMAX>::kSmemBytes;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE, NMAX>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  tc_gemm_kernel<MODE, NMAX><<<n_sm, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+}  // namespace
+}  // namespace tc
 
 cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Workspace& ws, int mode,
                            int n_sm, cudaStream_t s) {
@@ -616,7 +657,9 @@ cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Worksp
   a.I = sh.I;
   a.Is = sh.n_shared ? sh.Is : sh.I;
   a.Imax = imax_of(sh);
-  a.n_sh_chunks = sh.n_shared ? (T + kNMax - 1) / kNMax : 0;
+  // the front end (T <= 4) builds chunks of at most 32 rows, within 64
+  a.chunk = tc_chunk_rows(sh, T);
+  a.n_sh_chunks = sh.n_shared ? (T + a.chunk - 1) / a.chunk : 0;
   if (mode == 0) {
     a.aq[0][0] = m.gu_q[0][0];
     a.aq[0][1] = m.gu_q[0][1];
@@ -640,20 +683,9 @@ cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Worksp
     a.ks_r = sh.I / kKS;
     a.ks_s = a.Is / kKS;
   }
-  const void* fn = mode == 0 ? reinterpret_cast<const void*>(tc_gemm_kernel<0>)
-                             : reinterpret_cast<const void*>(tc_gemm_kernel<1>);
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[mode]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[mode] = true;
-  }
-  if (mode == 0)
-    tc_gemm_kernel<0><<<n_sm, kThreads, kSmemBytes, s>>>(a);
-  else
-    tc_gemm_kernel<1><<<n_sm, kThreads, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  if (a.chunk == 128)
+    return mode == 0 ? launch_gemm_inst<0, 128>(a, n_sm, s) : launch_gemm_inst<1, 128>(a, n_sm, s);
+  return mode == 0 ? launch_gemm_inst<0, 64>(a, n_sm, s) : launch_gemm_inst<1, 64>(a, n_sm, s);
 }
 
 }  // namespace moe

@@ -265,11 +265,12 @@ TC_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("T", [3, 5, 40, 150])
+@pytest.mark.parametrize("T", [3, 5, 40, 150, 300])
 def test_tc_grouped_gemm(m, shape, T):
     """T = 3 takes the small-batch routing front end where the shape allows
     (32 experts: 768 x 256 with a 512-wide shared expert), the five routing
-    kernels otherwise."""
+    kernels otherwise; T = 300 gives most shapes >= 64 rows per expert, which
+    selects 128-row chunks (N = 128 MMAs)."""
     H, I, E, k, ng, tg, ns, Is = shape
     sh = LayerShape(H, I, E, k, ng, tg, 2.5, n_shared=ns, shared_inter=Is)
     wl = Workload("tc", sh, T, 1, "bf16" if T % 2 else "f32", "zipf", 7700 + H + I + E + T)

@@ -6,6 +6,8 @@ glm_verify    same layer, T=4 correlated tokens per step (1 accepted + 3 drafts)
 glm_prefill   same layer, T=512 tokens in one call
 glm_stack     24 such layers resident, T=1, RMSNorm before each router and a
               residual add after each layer
+glm_prefill_uniform  the same layer, T=8192 without the Zipf skew (256 rows
+              per expert on average): the grouped GEMM where it is compute-bound
 
 GLM-5.2 layer geometry (256 routed experts, top-8, one shared expert,
 routed_scaling_factor, sigmoid noaux_tc routing): "GLM-5.2 on a 32 GB Mac"
@@ -77,6 +79,10 @@ CONFIGS = {
     "glm_prefill": Workload("glm_prefill", GLM, 512, 1, "bf16", "zipf", 1004),
     "glm_stack": Workload("glm_stack", GLM, 1, 16, "f32", "zipf", 5000,
                           layers=24, rmsnorm_eps=1e-5),
+    # calibration of the grouped GEMM where it is compute-bound: 8192 tokens
+    # without the Zipf skew, 256 plan rows per expert on average
+    "glm_prefill_uniform": Workload("glm_prefill_uniform", GLM, 8192, 1, "bf16", "uniform",
+                                    1005, extra={"bound": "tensor"}),
 }
 
 
