@@ -73,9 +73,10 @@ const char* check_weights(const moe_config_t* c, const moe_weights_t* w) {
 
 // Workspace layout: each buffer 256-byte aligned, in this order.
 struct Layout {
-  size_t off[21];
+  size_t off[23];
   size_t total;
   int hstride;
+  size_t dm_cpart;  // float offset of dm_cpart inside dm_part
 };
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -93,7 +94,14 @@ Layout layout_for(const moe_config_t* c) {
   // f16 rows and chunk list of the tensor-core path (shapes it takes only)
   const bool tc = c->hidden % 256 == 0 && c->inter % 256 == 0 &&
                   (!c->n_shared || c->shared_inter % 256 == 0);
-  const size_t sz[21] = {
+  // single-token tensor-core kernel (shapes it takes only)
+  const bool dm = c->hidden % 1024 == 0 && c->inter % 1024 == 0 &&
+                  (!c->n_shared || c->shared_inter == c->inter);
+  const int Is = c->n_shared ? c->shared_inter : 0;
+  const size_t dm_f = dm ? moe::dm_part_floats(c->hidden, c->inter, Is, c->top_k, c->n_shared) : 0;
+  const size_t dm_c = dm ? moe::dm_cnt_words(c->hidden, c->inter, Is, c->top_k, c->n_shared) : 0;
+  L.dm_cpart = dm_f - (dm ? static_cast<size_t>(c->top_k + c->n_shared) * (c->inter / 8) : 0);
+  const size_t sz[23] = {
       Tm * H * 4,            // xf
       Tm * E * 4,            // logits
       N * 4,                 // ids
@@ -115,9 +123,11 @@ Layout layout_for(const moe_config_t* c) {
       tc ? R * Imax * 2 : 0, // h16
       tc ? moe::tc_max_chunks(c->max_tokens, c->top_k, c->n_experts) * 16 : 0,  // chunks
       4,                     // n_rchunks
+      dm_f * 4,              // dm_part (+ dm_cpart)
+      dm ? dm_c * 4 + 512 : 0,  // dm_pub (512 B: generation, ids, weights), dm_cnt
   };
   size_t o = 0;
-  for (int i = 0; i < 21; ++i) {
+  for (int i = 0; i < 23; ++i) {
     L.off[i] = o;
     o += up256(sz[i]);
   }
@@ -148,6 +158,12 @@ Workspace carve(char* base, const Layout& L) {
   w.h16 = reinterpret_cast<__half*>(base + L.off[18]);
   w.chunks = reinterpret_cast<int4*>(base + L.off[19]);
   w.n_rchunks = reinterpret_cast<int32_t*>(base + L.off[20]);
+  w.dm_part = reinterpret_cast<float*>(base + L.off[21]);
+  w.dm_cpart = w.dm_part + L.dm_cpart;
+  w.dm_pub_gen = reinterpret_cast<unsigned long long*>(base + L.off[22]);
+  w.dm_pub_id = reinterpret_cast<int32_t*>(base + L.off[22] + 128);
+  w.dm_pub_w = reinterpret_cast<float*>(base + L.off[22] + 256);
+  w.dm_cnt = reinterpret_cast<unsigned*>(base + L.off[22] + 512);
   w.hstride = L.hstride;
   return w;
 }
@@ -353,6 +369,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
   // tensor-core path: TMA tensor maps over the weights and the f16 rows
   h->tc = moe::tc_path_ok(h->sh) ? moe::tc_create_maps(h->w, h->sh, h->ws, cfg->max_tokens)
                                  : nullptr;
+  // single-token tensor-core kernel: TMA tensor maps over the weights
+  h->dm = moe::dm_shape_ok(h->sh) ? moe::dm_create_maps(h->w, h->sh) : nullptr;
   *out = h;
   return MOE_OK;
 }
@@ -409,9 +427,16 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
   const Shape& sh = h->sh;
   const Workspace& ws = h->ws;
   cudaError_t e;
-  // one token: the fused single-kernel path when the shape fits it; else the
-  // tensor-core grouped GEMM when the shape fits that, else the SIMT path
-  if (moe::decode_path_ok(sh, T, h->n_sm)) {
+  // one token: a single-kernel path when the shape fits one (the SIMT
+  // kernel, measured faster where both fit; else the tensor-core one); else
+  // the tensor-core grouped GEMM when the shape fits that, else the SIMT path
+  const bool fused = moe::decode_path_ok(sh, T, h->n_sm);
+  if (!fused && moe::dm_path_ok(sh, T, h->n_sm, h->dm)) {
+    moe::PhaseMarker pm{tr.on() ? &Tracer::mark_cb : nullptr, &tr};
+    e = moe::launch_dm(*h->dm, h->w, sh, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
+                       h->n_sm, &h->decode_calls, pm, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (single-token tensor-core path)");
+  } else if (fused) {
     moe::PhaseMarker pm{tr.on() ? &Tracer::mark_cb : nullptr, &tr};
     e = moe::launch_decode(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
                            h->n_sm, &h->decode_calls, pm, s);
@@ -468,6 +493,7 @@ void moe_destroy(moe_layer_t* h) {
   cudaDeviceSynchronize();
   free_trace(h);
   moe::tc_destroy_maps(h->tc);
+  moe::dm_destroy_maps(h->dm);
   cudaFree(h->ws_base);
   if (cur >= 0) cudaSetDevice(cur);
   delete h;

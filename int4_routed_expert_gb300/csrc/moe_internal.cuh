@@ -33,6 +33,16 @@ struct Workspace {
   __half* h16;       // [Tm*k + Tm][Imax] f16 SwiGLU rows of the tensor-core path
   int4* chunks;      // routed chunks of <= 64 plan rows: {first row, rows, expert, 0}
   int32_t* n_rchunks;  // [1] number of routed chunks
+  // single-token tensor-core kernel (decode_mma.cu): two-part sums of the
+  // octets and tiles cut by CTA ranges [unit][2][16], per-octet corrections
+  // of the h fragments [slot][I/8], and the parts' counters (monotonic)
+  float* dm_part;
+  float* dm_cpart;
+  unsigned* dm_cnt;
+  // the selection published by CTA 0: generation word, ids, weights
+  unsigned long long* dm_pub_gen;
+  int32_t* dm_pub_id;
+  float* dm_pub_w;
   int hstride;       // row stride of hbuf in floats (>= Imax, multiple of 1024)
 };
 
@@ -48,6 +58,9 @@ struct Shape {
 
 namespace moe {
 struct TcMaps;  // TMA tensor maps of the tensor-core grouped GEMM (tc_gemm.cu)
+namespace dm {
+struct Maps;    // TMA tensor maps of the single-token tensor-core kernel (decode_mma.cu)
+}
 }
 
 struct moe_layer {
@@ -62,6 +75,7 @@ struct moe_layer {
   int n_sm;
   unsigned long long decode_calls;  // single-token barrier rounds so far (grid barrier targets)
   moe::TcMaps* tc;                  // NULL when the shape does not fit the tensor-core path
+  moe::dm::Maps* dm;                // NULL when the shape does not fit the single-token MMA kernel
   // phase tracing: trace_cap calls x (MOE_N_PHASES + 1) events, and per call
   // the phase id recorded after each launched phase
   cudaEvent_t* trace_ev;
@@ -138,6 +152,20 @@ struct PhaseMarker {
   }
 };
 bool decode_path_ok(const Shape& sh, int T, int n_sm);
+
+// Single-token kernel on the tensor cores (decode_mma.cu): H and I
+// multiples of 1024, the shared expert as wide as a routed one.
+bool dm_shape_ok(const Shape& sh);
+dm::Maps* dm_create_maps(const moe_weights_t& w, const Shape& sh);
+void dm_destroy_maps(dm::Maps* m);
+bool dm_path_ok(const Shape& sh, int T, int n_sm, const dm::Maps* maps);
+// workspace sizes of Workspace::dm_part (+ dm_cpart) and dm_cnt
+size_t dm_part_floats(int H, int I, int Is, int k, int n_shared);
+size_t dm_cnt_words(int H, int I, int Is, int k, int n_shared);
+cudaError_t launch_dm(const dm::Maps& maps, const moe_weights_t& w, const Shape& sh, const void* x,
+                      moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws, float* y,
+                      int accumulate, int n_sm, unsigned long long* calls, const PhaseMarker& pm,
+                      cudaStream_t s);
 // calls: the handle's count of grid-barrier rounds (read and advanced).
 cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const void* x,
                           moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,

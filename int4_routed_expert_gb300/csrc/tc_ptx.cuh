@@ -1,7 +1,7 @@
 // Inline-PTX building blocks of the tensor-core grouped GEMM: tensor memory
 // (TMEM) allocation, loads and stores, tcgen05.mma with the A operand in
 // TMEM and the B operand in shared memory, completion through mbarriers, and
-// 2-D TMA tensor loads.
+// 2-D and 3-D TMA tensor loads.
 //
 // Descriptor formats (PTX ISA, tcgen05 "shared memory descriptor" and
 // "instruction descriptor" for .kind::f16):
@@ -150,7 +150,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Same, with an L2 eviction-priority policy (createpolicy).
+// 3-D tensor tile load: box of the map at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Same as tma_load_2d, with an L2 eviction-priority policy (createpolicy).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
                                                  uint32_t bar, uint64_t policy) {
   asm volatile(

@@ -280,10 +280,20 @@ def test_tc_grouped_gemm(m, shape, T):
 
 
 def test_single_token_wide_intermediate(m):
-    """One token with an intermediate size the fused single-token kernel
-    does not keep in registers (I = 4096): the grouped GEMM takes it."""
-    sh = LayerShape(512, 4096, 32, 4, 4, 2, 2.5)
+    """One token with an intermediate size the SIMT single-token kernel
+    does not keep in registers (I = 4096): with H a multiple of 1024 the
+    tensor-core single-token kernel takes it; with H = 512 the grouped GEMM."""
+    sh = LayerShape(1024, 4096, 32, 4, 4, 2, 2.5)
     wl = Workload("tc_t1", sh, 1, 1, "bf16", "zipf", 7803)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 2)
+    m.moe_trace_enable(h.h, 1)
+    _run_full(m, wl, L, gen_activations(wl, 1, call=0), handle=h)
+    names, rows = m.moe_trace_read(h.h, 1)
+    assert {n for n, v in zip(names, rows[0]) if v > 0} == {"decode_fused"}
+    h.close()
+    sh = LayerShape(512, 4096, 32, 4, 4, 2, 2.5)
+    wl = Workload("tc_t1b", sh, 1, 1, "bf16", "zipf", 7804)
     L = gen_layer(wl, device=DEV)
     h = m.MoELayer(L, 2)
     m.moe_trace_enable(h.h, 1)
@@ -321,6 +331,69 @@ def test_tc_rmsnorm_residual(m):
                                     gamma=gamma.numpy(), resid=x0.numpy())
         err = resid_err_per_token(xd.cpu().numpy(), y_o, x0.numpy())
         assert err.max() <= TOL
+    h.close()
+
+
+# ------------------------------------- single-token tensor-core kernel ---
+
+DM_SHAPES = [
+    # H, I, E, k, n_group, topk_group, n_shared: H and I multiples of 1024
+    # with I beyond what the SIMT single-token kernel keeps in registers
+    # (I > 2048) take the single-token tensor-core kernel at T = 1
+    (1024, 3072, 32, 4, 4, 2, 1),    # fewer blocks and tiles than CTAs
+    (2048, 4096, 64, 6, 8, 3, 1),    # blocks and tiles cut by CTA ranges
+    (3072, 3072, 32, 8, 4, 2, 1),
+    (2048, 4096, 32, 4, 8, 4, 0),    # no shared expert
+]
+
+
+@pytest.mark.parametrize("shape", DM_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_single_token_tensor_core(m, shape, dtype):
+    H, I, E, k, ng, tg, ns = shape
+    sh = LayerShape(H, I, E, k, ng, tg, 2.5, n_shared=ns)
+    wl = Workload("dm", sh, 1, 1, dtype, "uniform", 9100 + H + I + E + k)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 1)
+    m.moe_trace_enable(h.h, 4)
+    # several calls of one handle: grid-barrier targets and part counters
+    for call in range(4):
+        _run_full(m, wl, L, gen_activations(wl, 1, call=call), handle=h)
+    names, rows = m.moe_trace_read(h.h, 4)
+    for row in rows:
+        assert {n for n, v in zip(names, row) if v > 0} == {"decode_fused"}
+    m.moe_trace_enable(h.h, 0)
+    h.close()
+
+
+def test_single_token_tensor_core_rmsnorm_residual(m):
+    sh = LayerShape(2048, 3072, 64, 6, 8, 3, 2.0)
+    wl = Workload("dm_resid", sh, 1, 1, "f32", "zipf", 9201, rmsnorm_eps=1e-5)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 4)
+    gamma = gen_norm_weight(wl, 0)
+    for call in range(3):
+        x0 = (gen_activations(wl, 1, call=call) * 2.0).float()
+        xd = x0.to(DEV)
+        h.forward(xd, y=xd, gamma=gamma.to(DEV), eps=RMS_EPS, accumulate=True)
+        torch.cuda.synchronize()
+        assert m.moe_device_status(h.h) == 0
+        y_o, _, _, _ = oracle_layer(wl, 0, router_of(wl), x0.numpy(), [0], eps=RMS_EPS,
+                                    gamma=gamma.numpy(), resid=x0.numpy())
+        err = resid_err_per_token(xd.cpu().numpy(), y_o, x0.numpy())
+        assert err.max() <= TOL, err
+    h.close()
+
+
+def test_single_token_tensor_core_deterministic(m):
+    sh = LayerShape(3072, 4096, 32, 8, 4, 2, 2.5)
+    wl = Workload("dm_det", sh, 1, 1, "bf16", "zipf", 9202)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 1)
+    x = gen_activations(wl, 1, call=0).to(DEV)
+    y1 = h.forward(x).clone()
+    for _ in range(3):
+        assert torch.equal(h.forward(x), y1)
     h.close()
 
 
