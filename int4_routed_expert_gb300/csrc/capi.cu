@@ -124,7 +124,7 @@ Layout layout_for(const moe_config_t* c) {
       tc ? moe::tc_max_chunks(c->max_tokens, c->top_k, c->n_experts) * 16 : 0,  // chunks
       4,                     // n_rchunks
       dm_f * 4,              // dm_part (+ dm_cpart)
-      dm ? dm_c * 4 + 512 : 0,  // dm_pub (512 B: generation, ids, weights), dm_cnt
+      512 + dm_c * 4,        // dm_pub (generation, ids, weights; both single-token kernels), dm_cnt
   };
   size_t o = 0;
   for (int i = 0; i < 23; ++i) {

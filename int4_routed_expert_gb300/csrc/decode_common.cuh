@@ -144,6 +144,11 @@ __device__ inline bool gbar_wait(unsigned long long* p, unsigned long long targe
   return ok != 0;
 }
 
+// Release store of a monotonic generation word (read with gbar_wait).
+__device__ __forceinline__ void publish_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 template <int EPL>
 __device__ __forceinline__ void select_token(const DecArgs& a, int t, int& id, float& w) {
   const size_t o = static_cast<size_t>(t) * a.sh.E;

@@ -307,19 +307,38 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
     __threadfence();
     __syncwarp();
     if (lane == 0) gbar_arrive(ws.gbar);
-    if (!gbar_wait(ws.gbar, a.gtarget, ws.dev_err)) {
-      failed = true;
-    } else {
-      // the plan: for one token the k selected experts are distinct, so the
-      // expert slot is the rank of its id
-      int id = 0;
-      float w = 0.0f;
+    bool ok = gbar_wait(ws.gbar, a.gtarget, ws.dev_err);
+    // CTA 0 selects the experts and publishes them; the other CTAs wait for
+    // the publication instead of selecting themselves (the same result), so
+    // that every CTA starts the routed rows at about the same time
+    int id = 0;
+    float w = 0.0f;
+    if (ok && b == 0) {
       switch (fast_select_epl(sh)) {
         case 1: select_token<1>(a, 0, id, w); break;
         case 2: select_token<2>(a, 0, id, w); break;
         case 4: select_token<4>(a, 0, id, w); break;
         default: select_token<8>(a, 0, id, w); break;
       }
+      if (lane < k) {
+        ws.dm_pub_id[lane] = id;
+        ws.dm_pub_w[lane] = w;
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) publish_u64(ws.dm_pub_gen, a.gtarget);
+    } else if (ok) {
+      ok = gbar_wait(ws.dm_pub_gen, a.gtarget, ws.dev_err);
+      if (ok && lane < k) {
+        id = __ldcg(ws.dm_pub_id + lane);
+        w = __ldcg(ws.dm_pub_w + lane);
+      }
+    }
+    if (!ok) {
+      failed = true;
+    } else {
+      // the plan: for one token the k selected experts are distinct, so the
+      // expert slot is the rank of its id
       int rank = 0;
       for (int j = 0; j < k; ++j) {
         const int o = __shfl_sync(0xffffffffu, id, j);

@@ -62,6 +62,7 @@ using dec::kMaxEntries;
 using dec::split_range;
 using dec::gbar_arrive;
 using dec::gbar_wait;
+using dec::publish_u64;
 
 constexpr int kNW = 7;                    // consumer warps (8 warps: 255 registers a thread)
 constexpr int kThreads = (kNW + 1) * 32;  // and the control warp
@@ -174,11 +175,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Release store of a monotonic generation word (read with gbar_wait).
-__device__ __forceinline__ void publish_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -39,7 +39,8 @@ struct Workspace {
   float* dm_part;
   float* dm_cpart;
   unsigned* dm_cnt;
-  // the selection published by CTA 0: generation word, ids, weights
+  // the selection of a single-token call, published by CTA 0 of either
+  // single-token kernel: generation word, ids, weights
   unsigned long long* dm_pub_gen;
   int32_t* dm_pub_id;
   float* dm_pub_w;
