@@ -38,9 +38,10 @@
 // of the activation) and give sum_i (u_i - 8) x_i, which the group's f16
 // scale multiplies into the row's fp32 sum.
 //
-// Roles: warps 0..kNW-1 consume items and issue their own copies; warp kNW
-// is the control warp (grid barriers, the selection and the plan, staging
-// the h fragments after barrier 2).
+// Roles: every warp consumes items and issues its own copies; warp 0 also
+// takes the control steps (grid barriers, the selection and the plan,
+// staging the h fragments after barrier 2) at points where the other warps
+// wait for them anyway.
 //
 // "GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri hierarchy", N1
 // (MoE bullet), N2 and "G2 - native GLM-5.2 correctness spine" (int4 gate/
@@ -64,8 +65,8 @@ using dec::gbar_arrive;
 using dec::gbar_wait;
 using dec::publish_u64;
 
-constexpr int kNW = 7;                    // consumer warps (8 warps: 255 registers a thread)
-constexpr int kThreads = (kNW + 1) * 32;  // and the control warp
+constexpr int kNW = 8;                    // warps (8: 255 registers a thread)
+constexpr int kThreads = kNW * 32;
 // the prologue's RMSNorm and router use warps 0..7 (one per logit segment)
 // and meet on a named barrier of those 256 threads
 static_assert(kThreads / 32 >= dec::kRouterWarps, "the router needs 8 warps in the CTA");
@@ -290,9 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L.bars);
   const uint32_t cb = smem_u32(bars + kNW * kStages);
-  // control barriers: plan ready, gate/up done, barrier 2 passed, h
-  // fragments landed, router rows landed
-  const uint32_t planbar = cb, gudone = cb + 8, b2pass = cb + 16, hbar = cb + 24, rbar = cb + 32;
+  // control barriers: plan ready, barrier 2 passed, h fragments landed,
+  // router rows landed
+  const uint32_t planbar = cb, b2pass = cb + 8, hbar = cb + 16, rbar = cb + 24;
   int sg0, sg1, rg0, rg1, d0, d1;
   phase_range(g.n_sg, g.UB, b, G, sg0, sg1);
   phase_range(g.n_rg, g.UB, b, G, rg0, rg1);
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNW * kStages; ++i) mbar_init(smem_u32(bars + i), 1);
-    for (int i = 0; i < 5; ++i) mbar_init(cb + 8 * i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(cb + 8 * i, 1);
     fence_barrier_init();
     // this CTA's router rows into the (still idle) ring area: the router
     // reads shared memory only, and no weight copy competes with the path
@@ -382,110 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
   __syncthreads();
   }
 
-  if (warp == kNW) {
-    // ================= control warp =================
-    // CTA 0 selects the experts and publishes them; the other CTAs wait for
-    // the publication instead of selecting themselves (the same result),
-    // so that every CTA starts streaming at the same time.
-
-    bool ok = __all_sync(0xffffffffu, pro_ok);
-    if (ok) {
-      // barrier 1: every router expert of the grid is scored
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) gbar_arrive(ws.gbar);
-      ok = gbar_wait(ws.gbar, a.gtarget, ws.dev_err);
-    }
-    int id = 0, rank = 0;
-    float w = 0.0f;
-    if (ok && b == 0) {
-      switch (fast_select_epl(sh)) {
-        case 1: dec::select_token<1>(a, 0, id, w); break;
-        case 2: dec::select_token<2>(a, 0, id, w); break;
-        case 4: dec::select_token<4>(a, 0, id, w); break;
-        default: dec::select_token<8>(a, 0, id, w); break;
-      }
-      if (lane < k) {
-        ws.dm_pub_id[lane] = id;
-        ws.dm_pub_w[lane] = w;
-      }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) publish_u64(ws.dm_pub_gen, a.gtarget);
-    } else if (ok) {
-      ok = gbar_wait(ws.dm_pub_gen, a.gtarget, ws.dev_err);
-      if (ok && lane < k) {
-        id = __ldcg(ws.dm_pub_id + lane);
-        w = __ldcg(ws.dm_pub_w + lane);
-      }
-    }
-    if (ok) {
-      // one token: the k experts are distinct; slot = rank of the id
-      for (int j = 0; j < k; ++j) {
-        const int o = __shfl_sync(0xffffffffu, id, j);
-        rank += (o < id) ? 1 : 0;
-      }
-      if (lane < k) {
-        s_pe[rank] = id;
-        s_pw[rank] = w;
-      }
-    }
-    // published even after a failed wait (the error word is set; the
-    // consumers then stream expert 0 instead of waiting)
-    __syncwarp();
-    if (lane == 0) mbar_arrive(planbar);
-    if (ok && b == 0) {
-      // the plan of the call (moe_forward's plan output), after the plan is
-      // published: not on the consumers' path
-      if (lane < k) {
-        ws.ids[lane] = id;
-        ws.topw[lane] = w;
-        ws.perm[rank] = lane;
-        ws.inv[lane] = rank;
-        ws.active[rank] = id;
-        ws.dslot[rank] = id;
-        ws.dslot[32 + rank] = rank;
-        ws.dslot[64 + rank] = 1;
-      }
-      if (lane == 0) *ws.n_active = k;
-      for (int e0 = 0; e0 < sh.E; e0 += 32) {
-        const int ex = e0 + lane;
-        int cnt = 0, off = 0;
-        for (int j = 0; j < k; ++j) {
-          const int o = __shfl_sync(0xffffffffu, id, j);
-          cnt += (o == ex) ? 1 : 0;
-          off += (o < ex) ? 1 : 0;
-        }
-        if (ex < sh.E) {
-          ws.counts[ex] = cnt;
-          ws.offsets[ex] = off;
-        }
-      }
-      if (lane == 0) ws.offsets[sh.E] = k;
-    }
-    bool ok2 = __all_sync(0xffffffffu, mbar_wait(gudone, 0, ws.dev_err));
-    if (ok && ok2) {
-      // barrier 2: every h row of the layer is written
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) gbar_arrive(ws.gbar);
-      gbar_wait(ws.gbar, a.gtarget2, ws.dev_err);
-    }
-    if (lane == 0) {
-      mbar_arrive(b2pass);
-      // the h fragments of all slots, written by the generic proxy in other
-      // CTAs, read here by the async proxy
-      fence_proxy_async_global();
-      fence_proxy_async_smem();
-      const uint32_t bytes = static_cast<uint32_t>(I / 32) * 64;
-      mbar_arrive_expect_tx(hbar, bytes * g.nslot);
-      const unsigned char* src = reinterpret_cast<const unsigned char*>(ws.h16);
-      for (int s = 0; s < g.nslot; ++s)
-        bulk_g2s(smem_u32(sm + L.bfr + static_cast<size_t>(s) * bytes),
-                 src + static_cast<size_t>(s) * bytes, bytes, hbar);
-    }
-    return;
-  }
 
   // ================= consumer warps =================
   const int nthr = kNW * 32;  // threads of the consumers' named barrier
@@ -606,11 +503,120 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
     planned = true;  // after a failed wait the slots read as expert 0
     if (!ok) failed = true;
   };
+  // Control steps, taken by consumer warp 0 while the other warps would
+  // wait anyway: barrier 1 and the plan (before any routed item), barrier 2
+  // and the h fragments (between the gate/up and the down items).
+  // CTA 0 selects the experts and publishes them; the other CTAs wait for
+  // the publication instead of selecting themselves (the same result), so
+  // that every CTA starts streaming at the same time.
+  bool ctl_ok = false;
+  auto control_plan = [&]() {
+    bool ok = __all_sync(0xffffffffu, pro_ok);
+    if (ok) {
+      // barrier 1: every router expert of the grid is scored
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) gbar_arrive(ws.gbar);
+      ok = gbar_wait(ws.gbar, a.gtarget, ws.dev_err);
+    }
+    int id = 0, rank = 0;
+    float w = 0.0f;
+    if (ok && b == 0) {
+      switch (fast_select_epl(sh)) {
+        case 1: dec::select_token<1>(a, 0, id, w); break;
+        case 2: dec::select_token<2>(a, 0, id, w); break;
+        case 4: dec::select_token<4>(a, 0, id, w); break;
+        default: dec::select_token<8>(a, 0, id, w); break;
+      }
+      if (lane < k) {
+        ws.dm_pub_id[lane] = id;
+        ws.dm_pub_w[lane] = w;
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) publish_u64(ws.dm_pub_gen, a.gtarget);
+    } else if (ok) {
+      ok = gbar_wait(ws.dm_pub_gen, a.gtarget, ws.dev_err);
+      if (ok && lane < k) {
+        id = __ldcg(ws.dm_pub_id + lane);
+        w = __ldcg(ws.dm_pub_w + lane);
+      }
+    }
+    if (ok) {
+      // one token: the k experts are distinct; slot = rank of the id
+      for (int j = 0; j < k; ++j) {
+        const int o = __shfl_sync(0xffffffffu, id, j);
+        rank += (o < id) ? 1 : 0;
+      }
+      if (lane < k) {
+        s_pe[rank] = id;
+        s_pw[rank] = w;
+      }
+    }
+    // published even after a failed wait (the error word is set; the
+    // consumers then stream expert 0 instead of waiting)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(planbar);
+    if (ok && b == 0) {
+      // the plan of the call (moe_forward's plan output), after the plan is
+      // published: not on the consumers' path
+      if (lane < k) {
+        ws.ids[lane] = id;
+        ws.topw[lane] = w;
+        ws.perm[rank] = lane;
+        ws.inv[lane] = rank;
+        ws.active[rank] = id;
+        ws.dslot[rank] = id;
+        ws.dslot[32 + rank] = rank;
+        ws.dslot[64 + rank] = 1;
+      }
+      if (lane == 0) *ws.n_active = k;
+      for (int e0 = 0; e0 < sh.E; e0 += 32) {
+        const int ex = e0 + lane;
+        int cnt = 0, off = 0;
+        for (int j = 0; j < k; ++j) {
+          const int o = __shfl_sync(0xffffffffu, id, j);
+          cnt += (o == ex) ? 1 : 0;
+          off += (o < ex) ? 1 : 0;
+        }
+        if (ex < sh.E) {
+          ws.counts[ex] = cnt;
+          ws.offsets[ex] = off;
+        }
+      }
+      if (lane == 0) ws.offsets[sh.E] = k;
+    }
+    ctl_ok = ok;
+  };
+  auto control_barrier2 = [&]() {
+    if (ctl_ok) {
+      // barrier 2: every h row of the layer is written
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) gbar_arrive(ws.gbar);
+      gbar_wait(ws.gbar, a.gtarget2, ws.dev_err);
+    }
+    if (lane == 0) {
+      mbar_arrive(b2pass);
+      // the h fragments of all slots, written by the generic proxy in other
+      // CTAs, read here by the async proxy
+      fence_proxy_async_global();
+      fence_proxy_async_smem();
+      const uint32_t bytes = static_cast<uint32_t>(I / 32) * 64;
+      mbar_arrive_expect_tx(hbar, bytes * g.nslot);
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(ws.h16);
+      for (int s = 0; s < g.nslot; ++s)
+        bulk_g2s(smem_u32(sm + L.bfr + static_cast<size_t>(s) * bytes),
+                 src + static_cast<size_t>(s) * bytes, bytes, hbar);
+    }
+  };
 
-
-  if (b == 0 && warp == 0) {
+  // no weight copy before the plan: streaming during the router -> barrier
+  // 1 -> selection path (even of the shared expert) measured slower
+  if (warp == 0) control_plan();
+  if (b == 0 && warp == 1) {
     // idle until the plan: fetch the selection code into the SM's
-    // instruction cache for the control warp (keys not final; result unused)
+    // instruction cache for warp 0 (keys not final; result unused)
     int id = 0;
     float w = 0.0f;
     switch (fast_select_epl(sh)) {
@@ -710,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
       }
     }
     tc::named_sync(kBarC, nthr);
-    if (threadIdx.x == 0) mbar_arrive(gudone);
   };
   // h fragments and their corrections, after grid barrier 2
   auto start_down = [&]() {
@@ -745,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) dm_kernel(const __grid_constant__
     if (j == ngu && !down) {
       flush();
       finish_gate_up();
+      if (warp == 0) control_barrier2();
       start_down();
       down = true;
       seg = 0;
