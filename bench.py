@@ -407,6 +407,23 @@ class OracleArm:
                 "oracle, fp32 accumulation")
 
 
+def max_over_ranks(values, world, device):
+    """The per-rank timings reduced to their maximum over the ranks (the
+    slowest rank sets the job's time); identity for one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tokens_per_s(world, tokens_per_step, steps, ms):
+    """Whole-job throughput: the tokens all ranks processed over the time."""
+    return world * tokens_per_step * steps / (ms / 1000.0)
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -502,14 +519,11 @@ def main():
         e2e_ms += run.timed_pass(e2e=True)
     run.check_status()
 
-    if world > 1:
-        t = torch.tensor([dev_ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dev_ms, e2e_ms = float(t[0]), float(t[1])
+    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], world, dev)
 
     tokens_step = wl.tokens_per_call * wl.calls
-    value = world * tokens_step * args.steps / (dev_ms / 1000.0)
-    e2e_value = world * tokens_step * args.steps / (e2e_ms / 1000.0)
+    value = job_tokens_per_s(world, tokens_step, args.steps, dev_ms)
+    e2e_value = job_tokens_per_s(world, tokens_step, args.steps, e2e_ms)
 
     phase_ms, n_phase, launches_step = run.traced_pass()
     n_act = run.active_experts()
