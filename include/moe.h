@@ -199,6 +199,20 @@ const char* moe_trace_phase_name(int phase);
  * kernel returned early; the outputs of that call are not valid. */
 moe_status_t moe_device_status(moe_layer_t* h, int32_t* flags);
 
+/* Self-test of the bounded waits behind bit 0 of moe_device_status, with no
+ * layer: one warp waits on something that never completes and gives up after
+ * about one second, the way the layer's kernels do, leaving the device usable.
+ *   which = 0: the grid-barrier wait (a counter in device memory that stays
+ *              below its target);
+ *   which = 1: an mbarrier wait (a phase nobody arrives on).
+ * Synchronous: allocates 256 bytes of device memory on the current device,
+ * launches one warp on the legacy default stream, waits for it, frees the
+ * memory and writes the kernel's error word to *flags (bit 0: the wait gave
+ * up).  Returns MOE_ERR_INVALID_ARG for which outside {0, 1} or flags NULL
+ * (before touching the device), MOE_ERR_CUDA if a CUDA call fails; messages
+ * through moe_last_error(NULL). */
+moe_status_t moe_selftest_bounded_wait(int which, int32_t* flags);
+
 /* Routing without any allocation (the pages have no counterpart: it serves
  * this library's callers, not a step of the method).
  *

@@ -7,7 +7,7 @@ fallback.
 Low-level functions mirror include/moe.h one to one:
     moe_layer_create, moe_route, moe_forward, moe_destroy, moe_last_error,
     moe_workspace_bytes, moe_trace_enable, moe_trace_read,
-    moe_trace_phase_name, moe_device_status
+    moe_trace_phase_name, moe_device_status, moe_selftest_bounded_wait
 ``MoELayer`` wraps a handle around torch tensors (device memory and streams
 only) for the tests and the benchmark.
 """
@@ -59,7 +59,8 @@ class moe_plan_t(C.Structure):
 
 EXPORTED = ("moe_layer_create", "moe_route", "moe_forward", "moe_destroy",
             "moe_last_error", "moe_workspace_bytes", "moe_trace_enable", "moe_trace_read",
-            "moe_trace_phase_name", "moe_device_status", "moe_route_noalloc")
+            "moe_trace_phase_name", "moe_device_status", "moe_route_noalloc",
+            "moe_selftest_bounded_wait")
 
 _lib = None
 
@@ -98,6 +99,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.moe_trace_phase_name.argtypes = [C.c_int]
     L.moe_device_status.restype = C.c_int
     L.moe_device_status.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
+    L.moe_selftest_bounded_wait.restype = C.c_int
+    L.moe_selftest_bounded_wait.argtypes = [C.c_int, C.POINTER(C.c_int32)]
     L.moe_route_noalloc.restype = C.c_int
     L.moe_route_noalloc.argtypes = [C.POINTER(moe_config_t), C.c_void_p, C.c_void_p, C.c_void_p,
                                     C.c_int, C.c_int, C.c_void_p, C.c_float,
@@ -163,6 +166,14 @@ def moe_device_status(h) -> int:
     """Device error flags of the handle (0 = fine); raises MoeError if set."""
     f = C.c_int32(0)
     _check(load().moe_device_status(h, C.byref(f)), h)
+    return f.value
+
+
+def moe_selftest_bounded_wait(which: int) -> int:
+    """Error word of a one-warp kernel whose wait never completes (0: grid
+    barrier, 1: mbarrier); bit 0 set when the wait gave up.  Takes ~1 s."""
+    f = C.c_int32(0)
+    _check(load().moe_selftest_bounded_wait(which, C.byref(f)))
     return f.value
 
 

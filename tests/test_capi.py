@@ -111,6 +111,17 @@ def test_null_handle(m):
     lib.moe_destroy(None)
 
 
+def test_bounded_wait_selftest_arguments(m):
+    """Invalid arguments are refused before the device is touched."""
+    lib = m.load()
+    flags = C.c_int32(7)
+    assert lib.moe_selftest_bounded_wait(2, C.byref(flags)) == -1
+    assert lib.moe_selftest_bounded_wait(-1, C.byref(flags)) == -1
+    assert lib.moe_selftest_bounded_wait(0, None) == -1
+    assert flags.value == 7
+    assert m.moe_last_error(None)
+
+
 def test_phase_names(m):
     names = [m.moe_trace_phase_name(p) for p in range(12)]
     assert all(names) and len(set(names)) == 12

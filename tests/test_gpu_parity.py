@@ -139,6 +139,17 @@ def test_device_status_clean(m):
     h.close()
 
 
+def test_bounded_wait_gives_up_and_device_stays_usable(m):
+    """A wait that can never complete (grid-barrier counter below its target,
+    mbarrier phase nobody arrives on) gives up after about one second, sets
+    bit 0 of the error word, and leaves the device usable."""
+    for which in (0, 1):
+        assert m.moe_selftest_bounded_wait(which) & 1 == 1
+    wl, L, h = _tiny_handle(m, 4)
+    _run_full(m, wl, L, gen_activations(wl, 3, call=2), handle=h)
+    h.close()
+
+
 def test_zero_tokens_is_noop(m):
     wl, L, h = _tiny_handle(m)
     x = torch.zeros(0, wl.shape.hidden, device=DEV)
