@@ -151,10 +151,23 @@ def phase_flops(phase, sh, T):
     return None
 
 
-def kernel_source_hash():
+# Sources each profiled kernel is compiled from: its DRAM traffic in
+# profiles/ncu_traffic.json is used only while these files are unchanged.
+KERNEL_SOURCES = {
+    "decode_fused": ("decode_fused.cuh", "decode_common.cuh", "decode_f1.cu", "decode_f2.cu",
+                     "decode.cu", "stream_common.cuh", "router_math.cuh", "moe_internal.cuh"),
+    "tc_gate_up": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh"),
+    "tc_down": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str):
+    files = KERNEL_SOURCES.get(kernel)
+    if files is None:
+        return None
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int4_routed_expert_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -162,13 +175,14 @@ def kernel_source_hash():
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    on the kernel's current sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("source_hash") != kernel_source_hash():
+    hk = kernel_source_hash(kernel)
+    if hk is None or t.get("source_hash", {}).get(kernel) != hk:
         return None
     return t.get("per_launch_bytes", {}).get(f"{workload}:{kernel}")
 
