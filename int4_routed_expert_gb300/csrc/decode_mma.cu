@@ -13,12 +13,13 @@
 //   down item     16 rows of one expert's down matrix (a "tile" of y), one
 //                 chunk of the intermediate dimension.
 // The units of each phase are split evenly over the CTAs (contiguous
-// ranges) and, inside a CTA, over the consumer warps (contiguous blocks):
-//   shared gate/up  (block, gate|up, chunk)        from the start
-//   routed gate/up  (slot, block, gate|up, chunk)  once the plan is known
+// ranges) and, inside a CTA, over the warps (contiguous blocks):
+//   shared gate/up  (block, gate|up, chunk)
+//   routed gate/up  (slot, block, gate|up, chunk)
 //   down            (tile, slot, chunk)            computed after grid barrier 2
 // where the slots are the selected experts in id order, then the shared
-// expert.  A warp keeps a running sum over its consecutive units of one
+// expert.  No weight copy is issued before the plan is known: streaming
+// during the router -> barrier 1 -> selection path measured slower.  A warp keeps a running sum over its consecutive units of one
 // block matrix (of one tile, each unit weighted by its slot's gate weight)
 // and writes one partial per block matrix (tile) to shared memory; the CTA
 // then adds each one's partials in warp order.  A block or tile cut by a CTA
@@ -134,7 +135,7 @@ __host__ __device__ inline Smem smem_of(const Shape& sh, const Geo& g, int seg_t
   return s;
 }
 
-// CTA b's range of a phase of n units in spans of `span` (octets, tiles):
+// CTA b's range of a phase of n units in spans of `span` (blocks, tiles):
 // split over min(G, n / span) CTAs, so that every part holds at least one
 // span and a span is cut at most once; the other CTAs get none.
 __host__ __device__ inline void phase_range(int n, int span, int b, int G, int& lo, int& hi) {
