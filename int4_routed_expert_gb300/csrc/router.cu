@@ -108,13 +108,14 @@ logits_kernel(const float* __restrict__ xf, int T, int H, const float* __restric
       }
     }
   }
+  // the 32 segment trees at once: lane L ends with value L = (a, b)
+  static_assert(kTE * kTT == 32, "one value per lane");
+  float v[32];
 #pragma unroll
   for (int a = 0; a < kTE; ++a)
 #pragma unroll
-    for (int b = 0; b < kTT; ++b) {
-      const float p = segment_tree(acc[a][b]);
-      if (lane == 0) segsum[warp][a * kTT + b] = p;
-    }
+    for (int b = 0; b < kTT; ++b) v[a * kTT + b] = acc[a][b];
+  segsum[warp][lane] = segment_tree32(v);
   __syncthreads();
   if (threadIdx.x < kTE * kTT) {
     const int a = threadIdx.x / kTT, b = threadIdx.x % kTT;

@@ -109,6 +109,28 @@ __device__ __forceinline__ float segment_tree(float p) {
   return p;
 }
 
+// segment_tree of 32 values at once: v[i] holds lane L's partial of value i;
+// on return lane L holds the full sum of value L.  Each step adds the halves
+// of the lanes L and L ^ d that lane L keeps (the lower half when bit d of L
+// is clear), so value i is summed over the same lane pairs in the same order
+// (d = 16, 8, 4, 2, 1) as segment_tree, bit for bit, with 31 shuffles
+// instead of 160.
+__device__ __forceinline__ float segment_tree32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int d = 16 >> s, n = 16 >> s;  // partner distance, values kept
+    const bool hi = (lane & d) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = hi ? v[n + i] : v[i];
+      const float send = hi ? v[i] : v[n + i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, d));
+    }
+  }
+  return v[0];
+}
+
 // Sum of the 8 segment sums (d = 4, 2, 1).
 __device__ __forceinline__ float segments_sum(const float* seg) {
   float a0 = __fadd_rn(seg[0], seg[4]), a1 = __fadd_rn(seg[1], seg[5]);
