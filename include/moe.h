@@ -196,8 +196,17 @@ const char* moe_trace_phase_name(int phase);
 /* Device-side status: copies the handle's device error word to *flags
  * (synchronous), clears it, and returns MOE_ERR_CUDA when it was non-zero.
  * Bit 0: a bounded wait inside a kernel gave up (about one second) and the
- * kernel returned early; the outputs of that call are not valid. */
+ * kernel returned early; the outputs of that call are not valid.  When the
+ * word was non-zero the handle's grid-barrier state is also reset, so that
+ * later calls run normally again (a call that gave up leaves it out of step). */
 moe_status_t moe_device_status(moe_layer_t* h, int32_t* flags);
+
+/* Self-test of the recovery above: puts the handle in the state a call that
+ * gave up leaves (its count of grid-barrier rounds one ahead of the device
+ * counter), so that the next single-token or small-batch call gives up after
+ * about one to two seconds with bit 0 set.  Host-side only; MOE_ERR_INVALID_ARG
+ * for a NULL handle. */
+moe_status_t moe_selftest_desync(moe_layer_t* h);
 
 /* Self-test of the bounded waits behind bit 0 of moe_device_status, with no
  * layer: one warp waits on something that never completes and gives up after

@@ -19,6 +19,7 @@ from .moe import (  # noqa: F401
     moe_layer_create,
     moe_route,
     moe_selftest_bounded_wait,
+    moe_selftest_desync,
     moe_route_noalloc,
     moe_trace_enable,
     moe_trace_phase_name,

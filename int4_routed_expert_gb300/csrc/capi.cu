@@ -587,14 +587,34 @@ moe_status_t moe_device_status(moe_layer_t* h, int32_t* flags) {
   if (e != cudaSuccess) return cuda_fail(h, e, "moe_device_status");
   *flags = v;
   if (v != 0) {
+    // A call that gave up left the grid-barrier counter and the two-part
+    // counters out of step with the handle's count of barrier rounds; every
+    // later single-token or small-batch call would wait for targets it cannot
+    // reach.  Start them all again from zero.
+    const Layout L = layout_for(&h->cfg);
     e = cudaMemset(h->ws.dev_err, 0, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemset(h->ws.gbar, 0, sizeof(unsigned long long));
+    if (e == cudaSuccess && L.off[22] < L.total)
+      e = cudaMemset(static_cast<char*>(h->ws_base) + L.off[22], 0, L.total - L.off[22]);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(h, e, "moe_device_status (clear)");
+    h->decode_calls = 0;
     set_err(h, "a bounded wait inside a kernel gave up (flags 0x%x); the outputs of the "
                "affected call are not valid",
             static_cast<unsigned>(v));
     return MOE_ERR_CUDA;
   }
+  return MOE_OK;
+}
+
+moe_status_t moe_selftest_desync(moe_layer_t* h) {
+  if (!h) {
+    set_err(nullptr, "moe_selftest_desync: handle is NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  // the state a call that gave up leaves: the next call's grid-barrier
+  // targets lie beyond what its CTAs' arrivals reach
+  h->decode_calls += 1;
   return MOE_OK;
 }
 

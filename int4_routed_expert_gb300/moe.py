@@ -7,7 +7,8 @@ fallback.
 Low-level functions mirror include/moe.h one to one:
     moe_layer_create, moe_route, moe_forward, moe_destroy, moe_last_error,
     moe_workspace_bytes, moe_trace_enable, moe_trace_read,
-    moe_trace_phase_name, moe_device_status, moe_selftest_bounded_wait
+    moe_trace_phase_name, moe_device_status, moe_selftest_bounded_wait,
+    moe_selftest_desync
 ``MoELayer`` wraps a handle around torch tensors (device memory and streams
 only) for the tests and the benchmark.
 """
@@ -60,7 +61,7 @@ class moe_plan_t(C.Structure):
 EXPORTED = ("moe_layer_create", "moe_route", "moe_forward", "moe_destroy",
             "moe_last_error", "moe_workspace_bytes", "moe_trace_enable", "moe_trace_read",
             "moe_trace_phase_name", "moe_device_status", "moe_route_noalloc",
-            "moe_selftest_bounded_wait")
+            "moe_selftest_bounded_wait", "moe_selftest_desync")
 
 _lib = None
 
@@ -99,6 +100,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.moe_trace_phase_name.argtypes = [C.c_int]
     L.moe_device_status.restype = C.c_int
     L.moe_device_status.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
+    L.moe_selftest_desync.restype = C.c_int
+    L.moe_selftest_desync.argtypes = [C.c_void_p]
     L.moe_selftest_bounded_wait.restype = C.c_int
     L.moe_selftest_bounded_wait.argtypes = [C.c_int, C.POINTER(C.c_int32)]
     L.moe_route_noalloc.restype = C.c_int
@@ -175,6 +178,12 @@ def moe_selftest_bounded_wait(which: int) -> int:
     f = C.c_int32(0)
     _check(load().moe_selftest_bounded_wait(which, C.byref(f)))
     return f.value
+
+
+def moe_selftest_desync(h) -> None:
+    """Put the handle in the state a call that gave up leaves (self-test of
+    the recovery in moe_device_status)."""
+    _check(load().moe_selftest_desync(h), h)
 
 
 def moe_trace_read(h, cap: int):

@@ -118,6 +118,7 @@ def test_bounded_wait_selftest_arguments(m):
     assert lib.moe_selftest_bounded_wait(2, C.byref(flags)) == -1
     assert lib.moe_selftest_bounded_wait(-1, C.byref(flags)) == -1
     assert lib.moe_selftest_bounded_wait(0, None) == -1
+    assert lib.moe_selftest_desync(None) == -1
     assert flags.value == 7
     assert m.moe_last_error(None)
 

@@ -150,6 +150,25 @@ def test_bounded_wait_gives_up_and_device_stays_usable(m):
     h.close()
 
 
+def test_handle_recovers_after_a_call_gives_up(m):
+    """A call whose grid barrier cannot complete gives up (bit 0); the status
+    call reports it and resets the barrier state; the next calls (one token,
+    then a small batch through the routing front end) are correct again."""
+    sh = LayerShape(1024, 512, 64, 6, 8, 3, 2.0)
+    wl = Workload("recover", sh, 1, 1, "bf16", "zipf", 7606)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 4)
+    _run_full(m, wl, L, gen_activations(wl, 1, call=0), handle=h)
+    m.moe_selftest_desync(h.h)
+    h.forward(gen_activations(wl, 1, call=1).to(DEV))
+    torch.cuda.synchronize()
+    with pytest.raises(m.MoeError):
+        m.moe_device_status(h.h)
+    _run_full(m, wl, L, gen_activations(wl, 1, call=2), handle=h)
+    _run_full(m, wl, L, gen_activations(wl, 3, call=3), handle=h)
+    h.close()
+
+
 def test_zero_tokens_is_noop(m):
     wl, L, h = _tiny_handle(m)
     x = torch.zeros(0, wl.shape.hidden, device=DEV)
