@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cuda.h>
+
 #include <new>
 
 #include "moe_internal.cuh"
@@ -68,6 +70,94 @@ const char* check_weights(const moe_config_t* c, const moe_weights_t* w) {
       if (!aligned16(p)) return "weight pointers must be 16-byte aligned";
     }
   }
+  return nullptr;
+}
+
+// cuMemGetAddressRange of the driver API: base and size of the allocation
+// holding a device address.
+using AddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+AddressRangeFn address_range_fn() {
+  static AddressRangeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<AddressRangeFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// The kernels and the TMA tensor maps read every byte of a weight array that
+// the shape implies, so an array must lie in device (or managed) memory of the
+// handle's device and inside allocations that hold all of it; anything else
+// would surface as an out-of-bounds access inside a kernel.  Adjacent
+// allocations are followed, since a virtual range mapped in pieces reports
+// one piece at a time.
+const char* check_extent(const void* p, size_t bytes, int device) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return "is not a CUDA pointer";
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return "is not device memory";
+  if (a.type == cudaMemoryTypeDevice && a.device != device)
+    return "is on another device than the current one";
+  const AddressRangeFn fn = address_range_fn();
+  if (!fn) return "cannot be checked (no cuMemGetAddressRange in the driver)";
+  CUdeviceptr cur = reinterpret_cast<CUdeviceptr>(p);
+  const CUdeviceptr end = cur + bytes;
+  while (cur < end) {
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (fn(&base, &size, cur) != CUDA_SUCCESS || base > cur || base + size <= cur)
+      return "extends past the end of its allocation";
+    cur = base + size;
+  }
+  return nullptr;
+}
+
+const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, int device,
+                                const char** which) {
+  const size_t E = c->n_experts, H = c->hidden, I = c->inter;
+  struct A {
+    const char* name;
+    const void* p;
+    size_t bytes;
+  };
+  const A routed[] = {{"router_w", w->router_w, E * H * 4},
+                      {"router_bias", w->router_bias, E * 4},
+                      {"gate_q", w->gate_q, E * I * H / 2},
+                      {"gate_s", w->gate_s, E * I * (H / 32) * 2},
+                      {"up_q", w->up_q, E * I * H / 2},
+                      {"up_s", w->up_s, E * I * (H / 32) * 2},
+                      {"down_q", w->down_q, E * H * I / 2},
+                      {"down_s", w->down_s, E * H * (I / 32) * 2}};
+  for (const A& x : routed)
+    if (const char* m = check_extent(x.p, x.bytes, device)) {
+      *which = x.name;
+      return m;
+    }
+  if (!c->n_shared) return nullptr;
+  const size_t Is = c->shared_inter;
+  const A shared[] = {{"sh_gate_q", w->sh_gate_q, Is * H / 2},
+                      {"sh_gate_s", w->sh_gate_s, Is * (H / 32) * 2},
+                      {"sh_up_q", w->sh_up_q, Is * H / 2},
+                      {"sh_up_s", w->sh_up_s, Is * (H / 32) * 2},
+                      {"sh_down_q", w->sh_down_q, H * Is / 2},
+                      {"sh_down_s", w->sh_down_s, H * (Is / 32) * 2}};
+  for (const A& x : shared)
+    if (const char* m = check_extent(x.p, x.bytes, device)) {
+      *which = x.name;
+      return m;
+    }
   return nullptr;
 }
 
@@ -355,6 +445,15 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
     cudaGetLastError();
     delete h;
     return MOE_ERR_OOM;
+  }
+  // (after the workspace allocation, which has made the device's context
+  // current on this thread for the driver query)
+  const char* which = "";
+  if (const char* m = check_weight_memory(cfg, w, h->device, &which)) {
+    set_err(nullptr, "weight array %s %s", which, m);
+    cudaFree(h->ws_base);
+    delete h;
+    return MOE_ERR_INVALID_ARG;
   }
   h->ws_bytes = L.total;
   h->ws = carve(static_cast<char*>(h->ws_base), L);

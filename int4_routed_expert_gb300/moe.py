@@ -230,6 +230,20 @@ class Plan:
     def c(self) -> moe_plan_t:
         return moe_plan_t(*(getattr(self, n).data_ptr() for n, _ in moe_plan_t._fields_))
 
+    def check(self, T: int, k: int, E: int, device) -> None:
+        """Raise unless every buffer is a contiguous int32/fp32 tensor on
+        ``device`` large enough for T tokens of this layer."""
+        import torch
+        need = {"topk_ids": (torch.int32, T * k), "topk_w": (torch.float32, T * k),
+                "counts": (torch.int32, E), "offsets": (torch.int32, E + 1),
+                "perm": (torch.int32, T * k), "active": (torch.int32, E),
+                "n_active": (torch.int32, 1)}
+        for name, (dt, n) in need.items():
+            t = getattr(self, name)
+            if t.device != device or t.dtype != dt or not t.is_contiguous() or t.numel() < n:
+                raise ValueError(f"plan.{name} must be a contiguous {dt} tensor on {device} "
+                                 f"with at least {n} elements")
+
 
 class MoELayer:
     """Handle + the tensors it borrows.  torch supplies memory and streams."""
@@ -261,6 +275,22 @@ class MoELayer:
             return MOE_BF16
         raise TypeError(f"x must be fp32 or bf16, got {x.dtype}")
 
+    def _check_x(self, x):
+        """x: a contiguous [T][hidden] fp32/bf16 tensor on a CUDA device; returns T."""
+        if not x.is_cuda or x.dim() != 2 or x.shape[1] != self.shape.hidden \
+                or not x.is_contiguous():
+            raise ValueError(f"x must be a contiguous CUDA tensor of shape [T, "
+                             f"{self.shape.hidden}], got {tuple(x.shape)} on {x.device}")
+        return x.shape[0]
+
+    def _check_vec(self, t, name: str, rows: int, device):
+        """t: a contiguous fp32 tensor on ``device`` with rows * hidden elements."""
+        import torch
+        if t.device != device or t.dtype != torch.float32 or not t.is_contiguous() \
+                or t.numel() != rows * self.shape.hidden:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor on {device} with "
+                             f"{rows} x {self.shape.hidden} elements")
+
     @staticmethod
     def _stream(stream) -> int:
         import torch
@@ -269,8 +299,11 @@ class MoELayer:
 
     def route(self, x, gamma=None, eps: float = 1e-5, plan: Plan | None = None,
               stream=None) -> Plan:
-        T = x.shape[0]
+        T = self._check_x(x)
+        if gamma is not None:
+            self._check_vec(gamma, "gamma", 1, x.device)
         plan = plan or Plan(T, self.shape.top_k, self.shape.n_experts, x.device)
+        plan.check(T, self.shape.top_k, self.shape.n_experts, x.device)
         pc = plan.c()
         moe_route(self.h, x.data_ptr(), self._dtype(x), T,
                   gamma.data_ptr() if gamma is not None else None, eps, pc,
@@ -280,9 +313,14 @@ class MoELayer:
     def forward(self, x, y=None, gamma=None, eps: float = 1e-5, accumulate: bool = False,
                 plan: Plan | None = None, stream=None):
         import torch
-        T = x.shape[0]
+        T = self._check_x(x)
         if y is None:
             y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=x.device)
+        self._check_vec(y, "y", T, x.device)
+        if gamma is not None:
+            self._check_vec(gamma, "gamma", 1, x.device)
+        if plan is not None:
+            plan.check(T, self.shape.top_k, self.shape.n_experts, x.device)
         pc = plan.c() if plan is not None else None
         moe_forward(self.h, x.data_ptr(), self._dtype(x), T, y.data_ptr(),
                     gamma.data_ptr() if gamma is not None else None, eps,

@@ -136,3 +136,31 @@ def test_binding_does_not_touch_the_oracle():
         text = open(path, errors="replace").read()
         assert not re.search(r"^\s*(import|from)\s+(oracle|numpy)\b", text, re.M), path
         assert "liboracle" not in text and "oracle.cpp" not in text, path
+
+
+def test_binding_checks_tensors_before_the_call(m):
+    """MoELayer refuses x, y, gamma and plan tensors that the kernels would
+    read or write out of bounds (wrong device, shape, dtype, layout or size),
+    on the host, before any C call."""
+    import torch
+
+    class _Shape:
+        hidden, top_k, n_experts = 256, 4, 16
+
+    lay = m.MoELayer.__new__(m.MoELayer)  # no handle: only the host checks run
+    lay.h = None
+    lay.shape = _Shape
+    with pytest.raises(ValueError):
+        lay._check_x(torch.zeros(2, 256))  # host tensor
+    cpu = torch.device("cpu")
+    lay._check_vec(torch.zeros(3, 256), "y", 3, cpu)
+    for bad in (torch.zeros(2, 256), torch.zeros(3, 256, dtype=torch.float64),
+                torch.zeros(256, 3).t()):
+        with pytest.raises(ValueError):
+            lay._check_vec(bad, "y", 3, cpu)
+    p = m.Plan(3, 4, 16, "cpu")
+    p.check(3, 4, 16, cpu)
+    p.check(2, 4, 16, cpu)  # more room than needed is fine
+    for args in ((4, 4, 16, cpu), (3, 4, 17, cpu), (3, 4, 16, torch.device("meta"))):
+        with pytest.raises(ValueError):
+            p.check(*args)

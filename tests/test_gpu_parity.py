@@ -139,6 +139,27 @@ def test_device_status_clean(m):
     h.close()
 
 
+def test_create_refuses_weights_outside_device_memory(m):
+    """A weight array in host memory (pageable or pinned) is refused at create
+    time with MOE_ERR_INVALID_ARG, naming the array; nothing is launched.  The
+    same weights on the device are accepted."""
+    wl = CONFIGS["tiny"]
+    L = gen_layer(wl, device=DEV)
+    cfg = m.moe.config_for(L.shape, 1)
+    nbytes = L.gate_q.numel() + 16
+    pageable = np.zeros(nbytes, dtype=np.uint8)
+    pinned = torch.zeros(nbytes, dtype=torch.uint8, pin_memory=True)
+    for addr in (pageable.ctypes.data, pinned.data_ptr()):
+        w = m.moe.weights_for(L)
+        w.gate_q = (addr + 15) & ~15
+        with pytest.raises(m.MoeError) as e:
+            m.moe_layer_create(cfg, w)
+        assert e.value.status == m.moe.MOE_ERR_INVALID_ARG
+        assert "gate_q" in str(e.value) and "device memory" in str(e.value)
+    h = m.moe_layer_create(cfg, m.moe.weights_for(L))
+    m.moe_destroy(h)
+
+
 def test_bounded_wait_gives_up_and_device_stays_usable(m):
     """A wait that can never complete (grid-barrier counter below its target,
     mbarrier phase nobody arrives on) gives up after about one second, sets
@@ -199,6 +220,18 @@ def test_capacity_and_argument_errors(m):
     with pytest.raises(m.MoeError) as ei:
         m.moe_forward(h.h, xx.data_ptr(), 7, 2, buf.data_ptr(), None, 0.0, 0, None, None)
     assert ei.value.status == -1
+    # the binding refuses tensors the kernels would read or write out of
+    # bounds, before the C call
+    bad = [dict(x=xx.cpu()), dict(x=xx[:, : H // 2]), dict(x=torch.randn(H, 2, device=DEV).t()),
+           dict(x=xx, y=torch.empty(1, H, device=DEV)),
+           dict(x=xx, y=torch.empty(2, H, device=DEV, dtype=torch.bfloat16)),
+           dict(x=xx, gamma=torch.ones(H // 2, device=DEV)),
+           dict(x=xx, plan=m.Plan(1, wl.shape.top_k, wl.shape.n_experts, DEV))]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            h.forward(**kw)
+    with pytest.raises(ValueError):
+        h.route(xx, plan=m.Plan(2, wl.shape.top_k, wl.shape.n_experts, "cpu"))
     h.close()
 
 
