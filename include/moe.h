@@ -140,7 +140,12 @@ typedef struct moe_layer moe_layer_t;
 /* Validate cfg and w, allocate the handle's device workspace (sized for
  * cfg->max_tokens) on the current CUDA device, and return the handle in
  * *out.  On failure *out is set to NULL and the message is available from
- * moe_last_error(NULL) on this thread. */
+ * moe_last_error(NULL) on this thread.
+ * Every weight array must lie in device (or managed) memory of the current
+ * device, inside allocations that hold all the bytes its shape implies
+ * (checked with cuMemGetAddressRange, following adjacent allocations);
+ * otherwise MOE_ERR_INVALID_ARG names the array.  The check cannot see a
+ * tensor that is too short inside a larger allocation. */
 moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
                               moe_layer_t** out);
 
