@@ -4,10 +4,15 @@ The oracle is the plain single-threaded C++ statement of the MoE layer in
 ``oracle/oracle.cpp``.  Only the tests, the smoke check and the benchmark's
 CPU-baseline leg may import this package.  It never imports the CUDA library
 and the CUDA library never imports it.
+
+``MOE_ORACLE_LIB``, when set, names another build of the oracle's source to
+load instead; the test that plants mistakes in the oracle uses it to run the
+pins against each altered copy.
 """
 from __future__ import annotations
 
 import ctypes as C
+import os
 
 import numpy as np
 
@@ -40,7 +45,7 @@ class _Layer(C.Structure):
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = os.environ.get("MOE_ORACLE_LIB") or _build.build()
         L = C.CDLL(path)
         L.oracle_router_exp.restype = C.c_float
         L.oracle_router_exp.argtypes = [C.c_float]

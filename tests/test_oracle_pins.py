@@ -370,6 +370,32 @@ def test_expert_reduces_to_integer_matvec():
     assert np.allclose(o, ref, rtol=1e-11, atol=1e-9)
 
 
+def test_expert_group_scales_per_row_and_matrix():
+    # integer weights and power-of-two scales that differ per row, per group of
+    # 32 and per matrix: every dequantised weight, product and sum is exact in
+    # float64, so the expert is the plain mat-vec SwiGLU of the dense matrices
+    # W[r, c] = q[r, c] * s[r, c // 32]; a scale read from the wrong row, group
+    # or matrix fails
+    H, I = 128, 64
+    rng = np.random.default_rng(17)
+    pow2 = np.array([0.25, 0.5, 1.0, 2.0])
+    Qg, Qu = rng.integers(-8, 8, (I, H)), rng.integers(-8, 8, (I, H))
+    Qd = rng.integers(-8, 8, (H, I))
+    Sg, Su = rng.choice(pow2, (I, H // 32)), rng.choice(pow2, (I, H // 32))
+    Sd = rng.choice(pow2, (H, I // 32))
+    x = rng.integers(-2, 3, H).astype(np.float32)
+    mats = (_pack(Qg), _f16bits(Sg), _pack(Qu), _f16bits(Su), _pack(Qd), _f16bits(Sd))
+    o = oracle.expert(x, I, mats, prec=1)
+    Wg = Qg * np.repeat(Sg, 32, axis=1)
+    Wu = Qu * np.repeat(Su, 32, axis=1)
+    Wd = Qd * np.repeat(Sd, 32, axis=1)
+    g = Wg @ x.astype(np.float64)
+    u = Wu @ x.astype(np.float64)
+    h = np.array([gi / (1 + math.exp(-gi)) * ui for gi, ui in zip(g, u)])
+    ref = Wd @ h
+    assert np.allclose(o, ref, rtol=1e-11, atol=1e-9 * np.abs(ref).max())
+
+
 def test_expert_linear_in_x_and_zero():
     from workloads import CONFIGS
     from workloads.gen import HostExpertCache
@@ -408,14 +434,16 @@ def test_layer_identical_experts_sum_to_rsf():
     shared = cache.expert(-1)
     rw, rb = gen_router(sh, w.seed, 0, "uniform")
     x = np.random.default_rng(14).standard_normal((3, sh.hidden)).astype(np.float32)
-    y, ids, wt, _ = oracle.moe_forward(sh, rw.numpy(), rb.numpy(), lambda e: one, shared, x,
-                                       prec=1)
-    for t in range(3):
-        e = oracle.expert(x[t], sh.inter, one, prec=1)
-        s = oracle.expert(x[t], sh.i_shared, shared, prec=1)
-        ref = float(wt[t].astype(np.float64).sum()) * e + s
-        assert abs(float(wt[t].astype(np.float64).sum()) - 2.5) < 1e-6
-        assert np.allclose(y[t], ref, rtol=1e-6, atol=1e-6 * np.abs(ref).max())
+    # both accumulations: fp64 (tight) and the fp32 layer the kernels match
+    for prec, tol in ((1, 1e-6), (0, 2e-5)):
+        y, ids, wt, _ = oracle.moe_forward(sh, rw.numpy(), rb.numpy(), lambda e: one, shared,
+                                           x, prec=prec)
+        for t in range(3):
+            e = oracle.expert(x[t], sh.inter, one, prec=1)
+            s = oracle.expert(x[t], sh.i_shared, shared, prec=1)
+            ref = float(wt[t].astype(np.float64).sum()) * e + s
+            assert abs(float(wt[t].astype(np.float64).sum()) - 2.5) < 1e-6
+            assert np.allclose(y[t], ref, rtol=tol, atol=tol * np.abs(ref).max())
 
 
 def test_layer_shared_only_when_routed_experts_are_zero():
