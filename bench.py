@@ -206,9 +206,10 @@ def phase_bytes(phase, sh, T, n_act, x_bytes):
     router = E * H * 4 + E * 4
     hrows = (T * k + T * ns) * sh.inter * 4
     if phase == "decode_fused":
+        # h stays between the kernel's two phases (L2), so it is not counted
         return (router + T * H * x_bytes + (n_act + ns) * expert_gate_up_bytes(sh)
                 + n_act * expert_down_bytes(sh) + ns * expert_down_bytes(sh, sh.i_shared)
-                + 2 * hrows + T * H * 4)
+                + T * H * 4)
     if phase == "gate_up":
         return (n_act + ns) * expert_gate_up_bytes(sh) + T * H * 4 + hrows
     if phase == "down":
