@@ -114,6 +114,34 @@ def test_shape_sweep(m, shape, T):
     _run_full(m, wl, L, x, max_tokens=max(T, 16))
 
 
+LIMIT_CASES = [
+    # H, I, E, k, n_group, topk_group, tokens per call: the largest hidden size
+    # on the single-token tensor-core kernel (T = 1) and the grouped GEMM
+    # (T = 2), and on the SIMT path (I = 96); the largest top_k (32 experts a
+    # token: the single-token SIMT kernel at T = 1, the grouped GEMM at T = 6);
+    # every expert selected (k = E); a single expert; a single group
+    (12288, 1024, 32, 4, 4, 2, (1, 2)),
+    (12288, 96, 16, 4, 4, 2, (1, 3)),
+    (1024, 512, 64, 32, 4, 4, (1, 6)),
+    (512, 256, 8, 8, 2, 2, (1, 4)),
+    (256, 256, 1, 1, 1, 1, (1, 3)),
+    (512, 256, 64, 8, 1, 1, (1, 2)),
+]
+
+
+@pytest.mark.parametrize("case", LIMIT_CASES, ids=lambda c: "x".join(map(str, c[:6])))
+def test_limits_and_degenerate_routing(m, case):
+    H, I, E, k, ng, tg, Ts = case
+    sh = LayerShape(H, I, E, k, ng, tg, 2.5)
+    wl = Workload("limits", sh, max(Ts), 1, "bf16", "zipf" if E >= 32 else "uniform",
+                  7900 + H + I + E + k)
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, max(Ts))
+    for T in Ts:
+        _run_full(m, wl, L, gen_activations(wl, T, call=T), handle=h)
+    h.close()
+
+
 def test_small_batch_with_rmsnorm(m):
     sh = LayerShape(1024, 512, 64, 6, 8, 3, 2.0)
     wl = Workload("norm", sh, 2, 1, "f32", "zipf", 7101, rmsnorm_eps=1e-5)
