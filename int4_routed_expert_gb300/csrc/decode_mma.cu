@@ -54,6 +54,7 @@
 #include <new>
 
 #include "decode_common.cuh"
+#include "smem_opt_in.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -981,12 +982,11 @@ cudaError_t launch_dm(const dm::Maps& maps, const moe_weights_t& w, const Shape&
   p.seg_sg = pl.seg_sg;
   p.seg_rg = pl.seg_rg;
   p.seg_d = pl.seg_d;
-  static size_t smem_set = 0;
-  if (pl.smem > smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        dm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+  static std::atomic<size_t> smem_set[kMaxDevices];
+  {
+    const cudaError_t e =
+        opt_in_smem(reinterpret_cast<const void*>(dm_kernel), smem_set, pl.smem);
     if (e != cudaSuccess) return e;
-    smem_set = pl.smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sm);

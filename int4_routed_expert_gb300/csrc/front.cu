@@ -18,6 +18,7 @@
 // and "G3 implementation status" (route the whole batch first; stable
 // row/rank batch union).
 #include "decode_common.cuh"
+#include "smem_opt_in.cuh"
 
 namespace moe {
 namespace dec {
@@ -296,13 +297,8 @@ namespace {
 // memory comes on top, so the 48 KB default is not enough at 48 KB).
 template <int RC>
 cudaError_t front_attr(size_t smem) {
-  static size_t set = 0;  // per instantiation
-  if (smem <= set) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(front_kernel<RC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-  if (e == cudaSuccess) set = smem;
-  return e;
+  static std::atomic<size_t> set[kMaxDevices];  // per instantiation
+  return opt_in_smem(reinterpret_cast<const void*>(front_kernel<RC>), set, smem);
 }
 }  // namespace
 }  // namespace dec

@@ -48,6 +48,7 @@
 #include <new>
 
 #include "moe_internal.cuh"
+#include "smem_opt_in.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -631,14 +632,11 @@ namespace tc {
 namespace {
 template <int MODE, int NMAX>
 cudaError_t launch_gemm_inst(const Args& a, int n_sm, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<size_t> attr_set[kMaxDevices];
   constexpr int smem = Cfg<NMAX>::kSmemBytes;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE, NMAX>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e =
+      opt_in_smem(reinterpret_cast<const void*>(tc_gemm_kernel<MODE, NMAX>), attr_set, smem);
+  if (e != cudaSuccess) return e;
   tc_gemm_kernel<MODE, NMAX><<<n_sm, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
