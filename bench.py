@@ -156,8 +156,10 @@ def phase_flops(phase, sh, T):
 KERNEL_SOURCES = {
     "decode_fused": ("decode_fused.cuh", "decode_common.cuh", "decode_f1.cu", "decode_f2.cu",
                      "decode.cu", "stream_common.cuh", "router_math.cuh", "moe_internal.cuh"),
-    "tc_gate_up": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh"),
-    "tc_down": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh"),
+    "tc_gate_up": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh",
+                   "smem_opt_in.cuh"),
+    "tc_down": ("tc_gemm.cu", "tc_ptx.cuh", "stream_common.cuh", "moe_internal.cuh",
+                "smem_opt_in.cuh"),
 }
 
 
