@@ -86,6 +86,17 @@ MUTANTS = {
                              "accf[r] = accf[r] + L->rsf * (float)o[r];"),
     "residual_dropped": ("y[(size_t)t * H + r] = resid ? base + v : v;",
                          "y[(size_t)t * H + r] = v;"),
+    # dropped last terms, saturation and rounding slips
+    "half_implicit_bit_dropped": ("(float)(mant | 0x400u)", "(float)mant"),
+    "exp_reduction_by_floor": ("std::nearbyint(t * kLog2e)", "std::floor(t * kLog2e)"),
+    "sigmoid_saturates_to_0": ("if (t < -32.0f) return 1.0f;", "if (t < -32.0f) return 0.0f;"),
+    "plan_offsets_start_at_count": ("offsets[0] = 0;", "offsets[0] = counts[0];"),
+    "last_gate_slot_skipped": ("for (int j = 0; j < k; ++j) {\n      const float g",
+                               "for (int j = 0; j + 1 < k; ++j) {\n      const float g"),
+    "expert_last_k_dropped": ("for (int k = 0; k < H; ++k) {\n      g = g",
+                              "for (int k = 0; k + 1 < H; ++k) {\n      g = g"),
+    "down_last_i_dropped": ("for (int i = 0; i < I; ++i) o = o",
+                            "for (int i = 0; i + 1 < I; ++i) o = o"),
 }
 
 
