@@ -11,9 +11,10 @@
 //   shared gate/up  x_hat (staged in shared memory by the prologue)
 //   shared down     barrier 1: every CTA has scored its router experts and
 //                   written its shared-expert h rows
-//   routed gate/up  the plan (warp 0 of the CTA derives it after barrier 1
-//                   and hands it to the other warps in shared memory; the
-//                   other warps stream shared down rows meanwhile)
+//   routed gate/up  the plan (after barrier 1, warp 0 of CTA 0 selects the
+//                   experts and publishes them; warp 0 of every CTA reads
+//                   them, derives the plan and hands it to the other warps
+//                   in shared memory; they stream shared down rows meanwhile)
 //   routed down     barrier 2: every routed h row is written
 // Down-projection results of the CTA's rows go to a (row, slot) table in
 // shared memory; at the end the CTA sums each row over the slots in a fixed
