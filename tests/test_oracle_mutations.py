@@ -97,6 +97,8 @@ MUTANTS = {
                               "for (int k = 0; k + 1 < H; ++k) {\n      g = g"),
     "down_last_i_dropped": ("for (int i = 0; i < I; ++i) o = o",
                             "for (int i = 0; i + 1 < I; ++i) o = o"),
+    "layer_rows_read_token_0": ("const float* xt = xh.data() + (size_t)t * H;",
+                                "const float* xt = xh.data();"),
 }
 
 

@@ -480,3 +480,23 @@ def test_layer_residual_and_rmsnorm():
                                          cache.expert(-1), h, eps=1e-5, resid=h)
     assert np.array_equal(ids0, ids1) and np.array_equal(w0, w1)
     assert np.array_equal(y1, (h + y0).astype(np.float32))
+
+
+def test_layer_rows_stable_alone_or_batched():
+    # a token's ids, weights and output are the same whether it runs alone
+    # (M = 1) or inside a batch of four (M = 4): rows never mix
+    from workloads import CONFIGS
+    from workloads.gen import HostExpertCache, gen_router
+    w = CONFIGS["tiny"]
+    sh = w.shape
+    cache = HostExpertCache(w)
+    rw, rb = gen_router(sh, w.seed, 0, "uniform")
+    x = np.random.default_rng(18).standard_normal((4, sh.hidden)).astype(np.float32)
+    y4, ids4, w4, _ = oracle.moe_forward(sh, rw.numpy(), rb.numpy(), cache.expert,
+                                         cache.expert(-1), x)
+    for t in range(4):
+        y1, ids1, w1, _ = oracle.moe_forward(sh, rw.numpy(), rb.numpy(), cache.expert,
+                                             cache.expert(-1), x[t:t + 1])
+        assert np.array_equal(ids1[0], ids4[t]) and np.array_equal(w1[0], w4[t])
+        assert np.array_equal(y1[0], y4[t])
+    assert len({tuple(r) for r in ids4.tolist()}) > 1  # the rows do differ
