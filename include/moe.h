@@ -242,18 +242,28 @@ moe_status_t moe_selftest_bounded_wait(int which, int32_t* flags);
  * without a layer handle).  It calls no cudaMalloc, cudaFree or allocating
  * library routine.
  *
- *   cfg       geometry; validated like moe_layer_create (MOE_ERR_UNSUPPORTED),
- *             max_tokens is not used
+ *   cfg       geometry; validated like moe_layer_create (MOE_ERR_UNSUPPORTED,
+ *             with the reason in moe_last_error(NULL)); max_tokens is not used
+ *             and may hold any value
  *   router_w  [E][H] fp32, router_bias [E] fp32, x [T][H] of dtype,
- *             rms_gamma [H] or NULL: device pointers, 16-byte aligned
- *   plan_out  as for moe_route (NULL members are kept in the scratch)
+ *             rms_gamma [H] or NULL: device pointers, 16-byte aligned.  Every
+ *             call checks that router_w and router_bias lie in device memory
+ *             of the current device, inside allocations that hold all E*H*4
+ *             and E*4 bytes (MOE_ERR_INVALID_ARG otherwise: a host pointer or
+ *             a short buffer would become an out-of-bounds read on the GPU);
+ *             x and rms_gamma are not checked this way
+ *   plan_out  as for moe_route (NULL members, or a NULL plan_out, are kept in
+ *             the scratch)
  * Limit: T * (hidden + n_experts) * 4 + 16 * T * top_k + 12 * n_experts, each
  * buffer rounded up to 256 bytes, must fit in the 2 MiB block (for example
  * T <= 64 at hidden = 6144, n_experts = 256, top_k = 8); larger T returns
  * MOE_ERR_CAPACITY with the sizes in moe_last_error(NULL).  T == 0 is a no-op.
  * The first call on a device looks up that device's block
  * (cudaGetSymbolAddress) with the device current; make that first call before
- * capturing any stream.  Nothing in the block needs to start at zero.  All
+ * capturing any stream.  A call whose stream is not being captured looks the
+ * address up again, so a device reset (after which the array can move) is
+ * safe once such a call has run; a call made during a capture uses the address
+ * of the last call that was not.  Nothing in the block needs to start at zero.  All
  * calls on one device share the block: two calls in flight at the same time
  * (on different streams or from different threads) race and give wrong
  * results, so serialise them.  Errors are reported through

@@ -395,6 +395,12 @@ void set_thread_error(const char* fmt, ...) {
   vsnprintf(g_err, sizeof(g_err), fmt, ap);
   va_end(ap);
 }
+
+const char* config_error(const moe_config_t* c) { return check_config(c); }
+
+const char* device_extent_error(const void* p, size_t bytes, int device) {
+  return check_extent(p, bytes, device);
+}
 }  // namespace moe
 
 extern "C" {

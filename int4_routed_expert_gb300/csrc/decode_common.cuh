@@ -303,12 +303,5 @@ cudaError_t launch_k(K kernel, int grid, int threads, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-template <typename K>
-cudaError_t set_smem_once(K kernel, size_t smem) {
-  if (smem <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem));
-}
-
 }  // namespace dec
 }  // namespace moe

@@ -29,6 +29,7 @@
 #pragma once
 
 #include "decode_common.cuh"
+#include "smem_opt_in.cuh"
 
 namespace moe {
 namespace dec {
@@ -585,12 +586,10 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
 template <int CPLH, int CPLI>
 cudaError_t launch_fused(const DecArgs& a, size_t smem, int n_sm, cudaStream_t s) {
   auto kern = dec_fused_kernel<CPLH, CPLI, kWarpsF, kStagesF>;
-  static size_t smem_max = 0;
-  if (smem > smem_max) {
-    const cudaError_t e = set_smem_once(kern, smem);
-    if (e != cudaSuccess) return e;
-    smem_max = smem;
-  }
+  // the opt-in is an attribute of the kernel on one device: kept per device
+  static std::atomic<size_t> smem_set[kMaxDevices];
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), smem_set, smem);
+  if (e != cudaSuccess) return e;
   return launch_k(kern, n_sm, kWarpsF * 32, smem, s, a, /*pdl=*/false, /*coop=*/true);
 }
 

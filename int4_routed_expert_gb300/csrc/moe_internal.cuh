@@ -91,6 +91,15 @@ namespace moe {
 // Sets the message moe_last_error(NULL) returns on this thread.
 void set_thread_error(const char* fmt, ...);
 
+// Why a configuration is rejected (NULL when it is valid), as moe_layer_create
+// and moe_workspace_bytes judge it.
+const char* config_error(const moe_config_t* c);
+
+// NULL when [p, p + bytes) lies in device (or managed) memory of `device`
+// inside allocations that hold all of it; else why not.  Needs a current
+// context on `device`.
+const char* device_extent_error(const void* p, size_t bytes, int device);
+
 // ---- launchers (each returns the cudaError_t of its launch) --------------
 
 // x (fp32 or bf16) -> xf fp32, optionally RMSNorm'd with gamma (fp64 sum of

@@ -19,15 +19,23 @@ void* g_addr[kMaxDevices] = {};
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Address of this device's scratch; looked up once per device, with that
-// device current.
-cudaError_t scratch_address(unsigned char** out) {
+// Address of this device's scratch, with that device current.  Looked up
+// once per device and cached for calls made while their stream is being
+// captured (a capture allows no module loading); every other call looks it
+// up again, so that a device reset, after which the module loads anew and
+// the array can move, leaves no stale address behind.
+cudaError_t scratch_address(cudaStream_t s, unsigned char** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    cs = cudaStreamCaptureStatusActive;  // unknown: do not touch the module
+  }
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (g_addr[dev] == nullptr) {
+  if (g_addr[dev] == nullptr || cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
@@ -45,10 +53,19 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* 
                                           const float* router_bias, const void* x,
                                           moe_dtype_t dtype, int T, const float* rms_gamma,
                                           float rms_eps, moe_plan_t* plan_out, void* stream) {
-  // moe_workspace_bytes validates the geometry without touching the device
-  if (!cfg || moe_workspace_bytes(cfg) == 0) {
-    moe::set_thread_error("moe_route_noalloc: unsupported or NULL configuration");
+  if (!cfg) {
+    moe::set_thread_error("moe_route_noalloc: cfg is NULL");
     return MOE_ERR_UNSUPPORTED;
+  }
+  {
+    // validated like moe_layer_create, except max_tokens, which this call
+    // does not use (T is limited by the scratch instead)
+    moe_config_t c = *cfg;
+    c.max_tokens = 1;
+    if (const char* m = moe::config_error(&c)) {
+      moe::set_thread_error("moe_route_noalloc: %s", m);
+      return MOE_ERR_UNSUPPORTED;
+    }
   }
   if (T < 0) {
     moe::set_thread_error("moe_route_noalloc: T must be >= 0");
@@ -90,8 +107,29 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* 
         T, total, kNoAllocScratchBytes);
     return MOE_ERR_CAPACITY;
   }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    // the router arrays are read in full by the logits and selection
+    // kernels: a host pointer or a short buffer must not reach them
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+      moe::set_thread_error("moe_route_noalloc: no usable CUDA device: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+    const char* which = "router_w";
+    const char* m = moe::device_extent_error(router_w, E * H * 4, dev);
+    if (!m) {
+      which = "router_bias";
+      m = moe::device_extent_error(router_bias, E * 4, dev);
+    }
+    if (m) {
+      moe::set_thread_error("moe_route_noalloc: %s %s", which, m);
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
   unsigned char* base = nullptr;
-  cudaError_t e = scratch_address(&base);
+  cudaError_t e = scratch_address(s, &base);
   if (e != cudaSuccess) {
     moe::set_thread_error("moe_route_noalloc: scratch address lookup failed: %s",
                           cudaGetErrorString(e));
@@ -118,7 +156,6 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* 
   const moe::Shape sh{cfg->hidden, cfg->inter, cfg->n_shared ? cfg->shared_inter : 0,
                       cfg->n_experts, cfg->top_k, cfg->n_group, cfg->topk_group,
                       cfg->n_shared, cfg->routed_scaling_factor};
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = moe::launch_prep(x, dtype, T, sh.H, rms_gamma, rms_eps, xf, s);
   if (e == cudaSuccess) e = moe::launch_router_logits(xf, T, sh.H, router_w, sh.E, logits, s);
   if (e == cudaSuccess) e = moe::launch_select(logits, router_bias, T, sh, ids, topw, s);

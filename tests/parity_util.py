@@ -23,6 +23,16 @@ def rel_err_per_token(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.abs(y - ref).max(axis=1) / den
 
 
+def elem_err_per_token(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """The element-wise companion figure (reported, not gated): per token, the
+    largest |y_i - ref_i| / max(|ref_i|, 1e-2 * max_j |ref_j|).  The floor keeps
+    elements near zero from dividing by almost nothing."""
+    y = np.asarray(y, np.float64).reshape(ref.shape[0], -1)
+    ref = np.asarray(ref, np.float64).reshape(ref.shape[0], -1)
+    floor = np.maximum(1e-2 * np.abs(ref).max(axis=1, keepdims=True), 1e-30)
+    return (np.abs(y - ref) / np.maximum(np.abs(ref), floor)).max(axis=1)
+
+
 def resid_err_per_token(y: np.ndarray, y_ref: np.ndarray, resid: np.ndarray) -> np.ndarray:
     """Error of a residual-form output y = resid + MoE(...).
 

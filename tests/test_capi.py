@@ -164,3 +164,18 @@ def test_binding_checks_tensors_before_the_call(m):
     for args in ((4, 4, 16, cpu), (3, 4, 17, cpu), (3, 4, 16, torch.device("meta"))):
         with pytest.raises(ValueError):
             p.check(*args)
+
+
+def test_route_noalloc_config_checks(m):
+    """moe_route_noalloc ignores max_tokens (any value is accepted) and
+    reports the configuration check's own reason for a bad geometry."""
+    f = m.load().moe_route_noalloc
+    for mt in (0, -5, 10 ** 6):
+        st = f(C.byref(_cfg(m, max_tokens=mt)), None, None, None, 0, 0, None, 0.0, None, None)
+        assert st == 0, (mt, m.moe_last_error(None))  # T == 0: a no-op after the checks
+    st = f(C.byref(_cfg(m, n_group=3, max_tokens=0)), None, None, None, 0, 0, None, 0.0, None,
+           None)
+    assert st == -2
+    assert "multiple of n_group" in m.moe_last_error(None)
+    st = f(None, None, None, None, 0, 0, None, 0.0, None, None)
+    assert st == -2 and "cfg is NULL" in m.moe_last_error(None)

@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import oracle
-from parity_util import (RMS_EPS, TOL, oracle_layer, rel_err_per_token, resid_err_per_token,
-                         router_of)
+from parity_util import (RMS_EPS, TOL, elem_err_per_token, oracle_layer, rel_err_per_token,
+                         resid_err_per_token, router_of)
 from workloads import CONFIGS
 from workloads.configs import LayerShape, Workload
 from workloads.gen import HostExpertCache, gen_activations, gen_layer, gen_norm_weight
@@ -44,7 +44,7 @@ def _check_plan(plan, ids_o, E):
 
 
 def _run_full(m, wl, L, x_cpu, *, layer=0, sample=None, gamma=None, max_tokens=None,
-              tol=TOL, cache=None, handle=None):
+              tol=TOL, cache=None, handle=None, report=None):
     """Forward x on the GPU with a plan; compare routing bit for bit and y."""
     sh = wl.shape
     T = x_cpu.shape[0]
@@ -69,6 +69,10 @@ def _run_full(m, wl, L, x_cpu, *, layer=0, sample=None, gamma=None, max_tokens=N
     tokens = list(range(T)) if sample is None else [t for t in sample if t < T]
     y_o, _, _, _ = oracle_layer(wl, layer, router, x32, tokens, eps=eps, gamma=gnp, cache=cache)
     err = rel_err_per_token(y.cpu().numpy()[tokens], y_o)
+    if report is not None:
+        # the gate is the per-token figure; the element-wise one is reported
+        ee = elem_err_per_token(y.cpu().numpy()[tokens], y_o)
+        report(f"{wl.name}_T{T}", float(err.max()), float(ee.max()))
     assert err.max() <= tol, err
     if own:
         h.close()
@@ -502,25 +506,50 @@ def _glm(name):
     return _GLM_CACHE[name]
 
 
-def test_glm_decode_tokens(m):
+@pytest.fixture
+def report(record_property):
+    """Records (and prints) the gated per-token error and the element-wise
+    companion figure of a parity case."""
+    def rec(name, per_token, elementwise):
+        record_property(f"{name}_per_token", per_token)
+        record_property(f"{name}_elementwise", elementwise)
+        print(f"parity {name}: per-token {per_token:.3e}, element-wise {elementwise:.3e}")
+    return rec
+
+
+def test_glm_decode_tokens(m, report):
+    """Outputs of three tokens against the oracle; the routing (ids, gate
+    weights, plan) of all 256 tokens of the benchmark's decode step."""
     wl, L, cache = _glm("glm_decode")
     h = m.MoELayer(L, 1)
     for call in (0, 1, 2):
         x = gen_activations(wl, 1, call=call)
-        _run_full(m, wl, L, x, cache=cache, handle=h)
+        _run_full(m, wl, L, x, cache=cache, handle=h, report=report)
+    router = router_of(wl, 0)
+    sh = wl.shape
+    plan = m.Plan(1, sh.top_k, sh.n_experts, DEV)
+    for call in range(wl.calls):
+        x = gen_activations(wl, 1, call=call)
+        h.forward(x.to(DEV), plan=plan)
+        _, _, ids_o, w_o = oracle.route(sh, router[0], router[1], x.float().numpy())
+        assert np.array_equal(plan.topk_ids.cpu().numpy(), ids_o), call
+        assert np.array_equal(plan.topk_w.cpu().numpy().view(np.uint32), w_o.view(np.uint32))
+        _check_plan(plan, ids_o, sh.n_experts)
+    assert m.moe_device_status(h.h) == 0
     h.close()
 
 
-def test_glm_verify_batch(m):
+def test_glm_verify_batch(m, report):
     wl, L, cache = _glm("glm_verify")
     x = gen_activations(wl, 4, call=0)
-    _run_full(m, wl, L, x, cache=cache)
+    _run_full(m, wl, L, x, cache=cache, report=report)
 
 
-def test_glm_prefill_sampled(m):
+def test_glm_prefill_sampled(m, report):
     wl, L, cache = _glm("glm_prefill")
     x = gen_activations(wl, 512, call=0)
-    _, plan, _ = _run_full(m, wl, L, x, sample=[0, 1, 77, 255, 300, 511], cache=cache)
+    _, plan, _ = _run_full(m, wl, L, x, sample=[0, 1, 77, 255, 300, 511], cache=cache,
+                           report=report)
     counts = plan.counts.cpu().numpy()
     assert counts.max() >= 40 and (counts == 0).sum() >= 1  # uneven, Zipf-skewed load
 

@@ -396,13 +396,35 @@ def test_expert_group_scales_per_row_and_matrix():
     assert np.allclose(o, ref, rtol=1e-11, atol=1e-9 * np.abs(ref).max())
 
 
+def _scaled(s_bits: np.ndarray, f: float) -> np.ndarray:
+    """fp16 scale bits multiplied by a power of two (exact for these scales)."""
+    out = (s_bits.view(np.float16).astype(np.float32) * np.float32(f)).astype(np.float16)
+    assert np.array_equal(out.astype(np.float32) / np.float32(f),
+                          s_bits.view(np.float16).astype(np.float32))
+    return out.view(np.uint16)
+
+
 def test_expert_linear_in_x_and_zero():
+    """Gate and up are linear maps of x: scaling x by a power of two a while
+    dividing the gate and up scales by a leaves every pre-activation, and so
+    the whole expert, unchanged bit for bit (each product and sum scales
+    exactly).  Down is linear in h: its scales times a give a times the
+    output, exactly.  x = 0 gives 0."""
     from workloads import CONFIGS
     from workloads.gen import HostExpertCache
     w = CONFIGS["tiny"]
-    mats = HostExpertCache(w).expert(3)
-    x = np.zeros(256, np.float32)
-    assert np.all(oracle.expert(x, 128, mats) == 0)
+    gq, gs, uq, us, dq, ds = HostExpertCache(w).expert(3)
+    x = np.random.default_rng(5).standard_normal(256).astype(np.float32)
+    base = oracle.expert(x, 128, (gq, gs, uq, us, dq, ds))
+    for a in (2.0, 0.5, 4.0):
+        xa = (x * np.float32(a)).astype(np.float32)
+        mats = (gq, _scaled(gs, 1 / a), uq, _scaled(us, 1 / a), dq, ds)
+        assert np.array_equal(oracle.expert(xa, 128, mats), base), a
+        # without the compensation the result changes (SwiGLU is not linear)
+        assert not np.array_equal(oracle.expert(xa, 128, (gq, gs, uq, us, dq, ds)), base)
+        out = oracle.expert(x, 128, (gq, gs, uq, us, dq, _scaled(ds, a)))
+        assert np.array_equal(out, base * a), a
+    assert np.all(oracle.expert(np.zeros(256, np.float32), 128, (gq, gs, uq, us, dq, ds)) == 0)
 
 
 def test_fp32_oracle_error_far_below_tolerance():

@@ -96,3 +96,55 @@ def test_noalloc_allocates_nothing_and_rejects_oversize(m):
     with pytest.raises(m.MoeError) as ei:
         _noalloc(m, cfg, R, big, None, 0.0, big_plan)
     assert ei.value.status == -3 and "2 MiB" in str(ei.value)
+
+
+def test_noalloc_partial_plan_and_argument_checks(m):
+    """Plan members left NULL (and a NULL plan) are kept in the scratch: the
+    members that are given still match the handle's route.  max_tokens is
+    ignored, and a router buffer shorter than E * H floats is refused before
+    any launch."""
+    import ctypes as C
+    wl = Workload("glm_like_partial", LayerShape(1024, 512, 64, 6, 8, 3, 2.5), 4, 1, "bf16",
+                  "zipf", 8300)
+    sh = wl.shape
+    L = gen_layer(wl, device=DEV)
+    h = m.MoELayer(L, 64)
+    T = 9
+    x = gen_activations(wl, T, call=3).to(DEV)
+    ref = h.route(x, plan=m.Plan(T, sh.top_k, sh.n_experts, DEV))
+    torch.cuda.synchronize()
+    cfg = m.moe.config_for(sh, 0)  # max_tokens = 0: not used by this call
+    stream = torch.cuda.current_stream().cuda_stream
+    full = m.Plan(T, sh.top_k, sh.n_experts, DEV)
+    part = full.c()
+    for name in ("topk_w", "offsets", "perm", "active", "n_active"):
+        setattr(part, name, None)
+    for t in (full.topk_ids, full.counts):
+        t.fill_(-1)
+    m.moe_route_noalloc(cfg, L.router_w.data_ptr(), L.router_b.data_ptr(), x.data_ptr(),
+                        m.MOE_BF16, T, None, 0.0, part, stream)
+    torch.cuda.synchronize()
+    assert torch.equal(full.topk_ids, ref.topk_ids)
+    assert torch.equal(full.counts, ref.counts)
+    # no plan at all, then the full plan again: still the handle's result
+    m.moe_route_noalloc(cfg, L.router_w.data_ptr(), L.router_b.data_ptr(), x.data_ptr(),
+                        m.MOE_BF16, T, None, 0.0, None, stream)
+    again = m.Plan(T, sh.top_k, sh.n_experts, DEV)
+    _noalloc(m, cfg, L, x, None, 0.0, again)
+    torch.cuda.synchronize()
+    _same_plan(ref, again)
+    # router arrays outside device memory are refused on the host (a short
+    # device buffer is refused the same way, but whether the addresses past a
+    # caching-allocator tensor belong to some allocation depends on the pool)
+    host_w = torch.zeros(sh.n_experts * sh.hidden, dtype=torch.float32).pin_memory()
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_route_noalloc(cfg, host_w.data_ptr(), L.router_b.data_ptr(), x.data_ptr(),
+                            m.MOE_BF16, T, None, 0.0, again.c(), stream)
+    assert ei.value.status == -1 and "router_w" in str(ei.value)
+    plain = C.create_string_buffer(sh.n_experts * 4 + 16)
+    addr = (C.addressof(plain) + 15) & ~15
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_route_noalloc(cfg, L.router_w.data_ptr(), addr, x.data_ptr(),
+                            m.MOE_BF16, T, None, 0.0, again.c(), stream)
+    assert ei.value.status == -1 and "router_bias" in str(ei.value)
+    h.close()
