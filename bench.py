@@ -14,6 +14,11 @@ served from L2.  `value` = tokens of all ranks / max-over-ranks device time.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (weak scaling, no data-path collective: the layer does not shard).
 `--impl reference` times the CPU oracle (the reference arm) on rank 0.
+
+Without --workload the run measures glm_decode (the headline line) and then,
+at one GPU, glm_verify, glm_prefill, glm_stack and glm_prefill_uniform as
+sub-records of the same line, each timed for at least 1.5 s with its own
+clock record.
 """
 from __future__ import annotations
 
@@ -44,8 +49,8 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons; only the samples
-    taken between mark_start() and mark_stop() are summarised."""
+    """nvidia-smi samples of SM clock and throttle reasons, summarised over a
+    given window of the run (one timed region)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -56,7 +61,6 @@ class ClockSampler:
         self.samples = []
         self.proc = None
         self.thread = None
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -76,11 +80,9 @@ class ClockSampler:
             if len(parts) >= 7:
                 self.samples.append((time.monotonic(), parts))
 
-    def mark_start(self):
-        self.t0 = time.monotonic()
-
-    def mark_stop(self):
-        self.t1 = time.monotonic()
+    @staticmethod
+    def now():
+        return time.monotonic()
 
     def wait_first(self, timeout=10.0):
         end = time.monotonic() + timeout
@@ -97,13 +99,13 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0, t1):
+        """Median SM clock and the throttle reasons seen in [t0, t1]."""
         sm = []
         mx = None
         reasons = set()
         names = ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
-        inside = [p for t, p in self.samples
-                  if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        inside = [p for t, p in list(self.samples) if t0 <= t <= t1]
         for p in inside:
             try:
                 sm.append(float(p[0]))
@@ -468,47 +470,71 @@ def run_reference(args, wl):
 
 # -------------------------------------------------------------- main arm ----
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="glm_decode",
-                    choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
-                             "glm_prefill_uniform"])
-    ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
-    ap.add_argument("--calls", type=int, default=None, help="override calls per step")
-    ap.add_argument("--layers", type=int, default=None, help="override stacked layers")
-    ap.add_argument("--tokens", type=int, default=None,
-                    help="override tokens per call (profiling only)")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    wl = make_workload(args.workload, args.experts, args.calls, args.tokens)
+# The workloads the default run measures after the headline (one process, one
+# after another, each layer stack freed before the next is generated).
+SUB_WORKLOADS = ("glm_verify", "glm_prefill", "glm_stack", "glm_prefill_uniform")
+# A sub-record's timed region lasts at least this long, so that the 200 ms
+# clock sampler sees several samples under load.
+SUB_MIN_TIMED_S = 1.5
 
-    if args.impl == "reference":
-        run_reference(args, wl)
-        return
+# Tokens a verify forward emits on average with the production MTP draft
+# ("GLM-5.2 on a 32 GB Mac - native MLX port of the Colibri hierarchy", G4:
+# 2.065 per forward; G5: 2.286).
+ACCEPTED_PER_VERIFY = (("G4", 2.065), ("G5", 2.286))
+
+
+def host_cpu():
+    """The host's logical CPU count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return os.cpu_count(), model or "unknown"
+
+
+def union_bytes_per_call(wl, n_act, x_bytes):
+    """HBM bytes of one call that streams each selected expert once: the
+    distinct experts of the call plus the shared one, the router, x and y."""
+    sh = wl.shape
+    T, H = wl.tokens_per_call, sh.hidden
+    ns = 1 if sh.n_shared else 0
+    return ((n_act + ns) * (expert_gate_up_bytes(sh) + expert_down_bytes(sh))
+            + sh.n_experts * H * 4 + sh.n_experts * 4 + T * H * x_bytes + T * H * 4)
+
+
+def measure(args, wl, dev, world, steps, warmup, clocks, min_timed_s=0.0, layers=None,
+            experts=None, tokens=None):
+    """One workload, timed: the fields of its bench line.
+
+    steps: the timed steps (raised, when min_timed_s is given, until the timed
+    region lasts at least that long, judged from the warm-up passes)."""
+    import math
 
     import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = f"cuda:{local}"
-    torch.cuda.set_device(dev)
 
-    import __graft_entry__
-    __graft_entry__.build()
-
-    run = GpuRun(wl, dev, args.layers)
+    run = GpuRun(wl, dev, layers)
     sh = wl.shape
-    clocks = ClockSampler(local)
-    clocks.start()
-    for _ in range(max(args.warmup, 3)):
-        run.timed_pass()
+    warm_ms = []
+    for _ in range(max(warmup, 3)):
+        warm_ms.append(run.timed_pass())
     run.check_status()
+    if min_timed_s > 0:
+        step_s = min(warm_ms) / 1000.0
+        steps = max(steps, int(math.ceil(min_timed_s / max(step_s, 1e-6))))
     clocks.wait_first()
 
     def barrier():
@@ -517,13 +543,12 @@ def main():
         torch.cuda.synchronize()
 
     barrier()
-    clocks.mark_start()
+    t_start = clocks.now()
     dev_ms = 0.0
-    for _ in range(args.steps):
+    for _ in range(steps):
         dev_ms += run.timed_pass()
     barrier()
-    clocks.mark_stop()
-    clocks.stop()
+    t_stop = clocks.now()
     run.check_status()
 
     # steady state without the L2 flush (weights of popular experts may stay in L2)
@@ -532,15 +557,15 @@ def main():
     # end to end: inputs copied from pinned host memory and outputs read back
     # inside each forward's events
     e2e_ms = 0.0
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_ms += run.timed_pass(e2e=True)
     run.check_status()
 
     dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], world, dev)
 
     tokens_step = wl.tokens_per_call * wl.calls
-    value = job_tokens_per_s(world, tokens_step, args.steps, dev_ms)
-    e2e_value = job_tokens_per_s(world, tokens_step, args.steps, e2e_ms)
+    value = job_tokens_per_s(world, tokens_step, steps, dev_ms)
+    e2e_value = job_tokens_per_s(world, tokens_step, steps, e2e_ms)
 
     phase_ms, n_phase, launches_step = run.traced_pass()
     n_act = run.active_experts()
@@ -558,72 +583,166 @@ def main():
         if b:
             kernels[name]["algorithmic_bytes"] = b
             kernels[name]["achieved_gbs"] = round(b / (avg / 1000.0) / 1e9, 1)
+        f = phase_flops(name, sh, T)
+        if f:
+            kernels[name]["tflops"] = round(f / (avg / 1000.0) / 1e12, 1)
     layer_bytes = sum(phase_bytes(n, sh, T, n_act, run.x_bytes) or 0 for n in phase_ms)
-    ms_per_call = dev_ms / (args.steps * wl.calls * max(1, run.n_layers))
+    ms_per_call = dev_ms / (steps * wl.calls * max(1, run.n_layers))
     layer_gbs = layer_bytes / (ms_per_call / 1000.0) / 1e9
+
+    achieved = kb / (per_launch_ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant,
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": ncu_traffic(dominant, workload_key(wl, experts, tokens)),
+                "algorithmic_bytes_per_launch": kb,
+                "avg_launch_us": round(1000 * per_launch_ms, 3),
+                "duration_source": "CUDA events between the kernels in a traced pass "
+                                   "of the same step right after the timed region"}
+    fl = phase_flops(dominant, sh, T)
+    if wl.extra.get("bound") == "tensor" and fl:
+        tpeak, tkind = measured_tensor_peak()
+        tach = fl / (per_launch_ms / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(tach, 1),
+                    "peak": tpeak, "unit": "TFLOP/s", "frac": round(tach / tpeak, 4),
+                    "peak_kind": tkind, "traffic": roofline["traffic"],
+                    "algorithmic_flops_per_launch": fl,
+                    "avg_launch_us": roofline["avg_launch_us"],
+                    "duration_source": roofline["duration_source"],
+                    "hbm": {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}}
+    rec = {
+        "value": value, "unit": UNIT, "steps": steps, "warmup": max(warmup, 3),
+        "ms_per_step": dev_ms / steps, "timed_s": round(dev_ms / 1000.0, 3),
+        "config": {
+            "workload": wl.name, "hidden": sh.hidden, "inter": sh.inter,
+            "n_experts": sh.n_experts, "top_k": sh.top_k, "layers": run.n_layers,
+            "tokens_per_call": T, "calls_per_step": wl.calls,
+            "tokens_per_step": tokens_step, "x_dtype": "f32" if run.norm else wl.x_dtype,
+            "weights": "int4 offset-binary, group 32, fp16 scales",
+            "l2": "flushed (512 MiB read) before every forward, outside the events",
+            "unflushed_tokens_per_s": round(tokens_step / (unflushed_ms / 1000.0), 1),
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": roofline,
+        "layer_hbm": {"bytes_per_call": layer_bytes, "gbs": round(layer_gbs, 1),
+                      "pct_of_8tbs": round(100 * layer_gbs / NOMINAL_HBM_GBS, 1),
+                      "frac_of_measured": round(layer_gbs / peak, 4),
+                      "mean_active_experts": n_act},
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(run.x[0].numel() * run.x_bytes * wl.calls),
+                "d2h_bytes_per_step": int(run.y[0].numel() * 4 * wl.calls)},
+        "gpu_launches": launches_step * steps,
+        "clocks": clocks.summary(t_start, t_stop),
+    }
+    if T > 1 and T <= 4:
+        # a verify forward: bytes of the expert union it streams, per step,
+        # per verified token and per emitted token
+        ub = union_bytes_per_call(wl, n_act, run.x_bytes)
+        calls_per_s = value / T
+        rec["verify"] = {
+            "union_bytes_per_call": ub, "bytes_per_step": ub * wl.calls,
+            "bytes_per_verified_token": ub / T,
+            "union_gbs": round(ub * calls_per_s / 1e9, 1),
+            "union_frac_of_measured": round(ub * calls_per_s / 1e9 / peak, 4),
+            "per_emitted_token": {
+                f"{src} ({acc} tokens per forward)": {
+                    "bytes": round(ub / acc, 1),
+                    "emitted_tokens_per_s": round(calls_per_s * acc, 1)}
+                for src, acc in ACCEPTED_PER_VERIFY},
+            "source": "GLM-5.2 on a 32 GB Mac, G4 and G5 (accepted tokens per verify forward)",
+        }
+    del run
+    torch.cuda.empty_cache()
+    return rec
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=None,
+                    choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
+                             "glm_prefill_uniform"],
+                    help="one workload only (default: glm_decode, then the other GLM "
+                         "workloads as sub-records)")
+    ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
+    ap.add_argument("--calls", type=int, default=None, help="override calls per step")
+    ap.add_argument("--layers", type=int, default=None, help="override stacked layers")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override tokens per call (profiling only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-records", action="store_true")
+    args = ap.parse_args()
+    single = args.workload is not None
+    name = args.workload or "glm_decode"
+    wl = make_workload(name, args.experts, args.calls, args.tokens)
+
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    rec = measure(args, wl, dev, world, args.steps, args.warmup, clocks, layers=args.layers,
+                  experts=args.experts, tokens=args.tokens)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
+        T = wl.tokens_per_call
         n_calls = 8 if T == 1 else 2
         arm = OracleArm(wl, n_calls)
         s_tok = sum(arm.run(c) for c in range(n_calls)) / n_calls
-        cpu = {"value": 1.0 / s_tok, "unit": UNIT, "cores": 1, "kind": "oracle",
+        nproc, model = host_cpu()
+        cpu = {"value": 1.0 / s_tok, "unit": UNIT, "cores": 1, "host_nproc": nproc,
+               "cpu_model": model, "kind": "oracle",
                "sample": f"{n_calls} call(s): " + arm.describe()}
 
+    subs = None
+    if not single and not args.no_sub_records and world == 1:
+        subs = {}
+        for sub in SUB_WORKLOADS:
+            swl = make_workload(sub)
+            subs[sub] = measure(args, swl, dev, world, 1, args.warmup, clocks,
+                                min_timed_s=SUB_MIN_TIMED_S)
+    clocks.stop()
+
     if rank == 0:
-        achieved = kb / (per_launch_ms / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": dominant,
-                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                    "traffic": ncu_traffic(dominant, workload_key(wl, args.experts, args.tokens)),
-                    "algorithmic_bytes_per_launch": kb,
-                    "avg_launch_us": round(1000 * per_launch_ms, 3),
-                    "duration_source": "CUDA events between the kernels in a traced pass "
-                                       "of the same step right after the timed region"}
-        fl = phase_flops(dominant, sh, T)
-        if wl.extra.get("bound") == "tensor" and fl:
-            tpeak, tkind = measured_tensor_peak()
-            tach = fl / (per_launch_ms / 1000.0) / 1e12
-            roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(tach, 1),
-                        "peak": tpeak, "unit": "TFLOP/s", "frac": round(tach / tpeak, 4),
-                        "peak_kind": tkind, "traffic": roofline["traffic"],
-                        "algorithmic_flops_per_launch": fl,
-                        "avg_launch_us": roofline["avg_launch_us"],
-                        "duration_source": roofline["duration_source"],
-                        "hbm": {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s"}}
-        for name in kernels:
-            f = phase_flops(name, sh, T)
-            if f:
-                kernels[name]["tflops"] = round(f / (kernels[name]["avg_us"] / 1e6) / 1e12, 1)
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": dev_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32",
+            "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world,
+            "steps": rec["steps"], "warmup": rec["warmup"], "ms_per_step": rec["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded int4 weights, fp16 scales, Zipf router bias)",
-            "config": {
-                "workload": wl.name, "hidden": sh.hidden, "inter": sh.inter,
-                "n_experts": sh.n_experts, "top_k": sh.top_k, "layers": run.n_layers,
-                "tokens_per_call": T, "calls_per_step": wl.calls,
-                "tokens_per_step": tokens_step, "x_dtype": "f32" if run.norm else wl.x_dtype,
-                "weights": "int4 offset-binary, group 32, fp16 scales",
-                "l2": "flushed (512 MiB read) before every forward, outside the events",
-                "unflushed_tokens_per_s": round(tokens_step / (unflushed_ms / 1000.0), 1),
-                "parallelism": f"replicas x{world}",
-            },
-            "roofline": roofline,
-            "layer_hbm": {"bytes_per_call": layer_bytes, "gbs": round(layer_gbs, 1),
-                          "pct_of_8tbs": round(100 * layer_gbs / NOMINAL_HBM_GBS, 1),
-                          "frac_of_measured": round(layer_gbs / peak, 4),
-                          "mean_active_experts": n_act},
-            "kernels": kernels,
+            "config": rec["config"],
+            "roofline": rec["roofline"],
+            "layer_hbm": rec["layer_hbm"],
+            "kernels": rec["kernels"],
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT,
-                    "h2d_bytes_per_step": int(run.x[0].numel() * run.x_bytes * wl.calls),
-                    "d2h_bytes_per_step": int(run.y[0].numel() * 4 * wl.calls)},
-            "gpu_launches": launches_step * args.steps,
-            "clocks": clocks.summary(),
+            "e2e": rec["e2e"],
+            "gpu_launches": rec["gpu_launches"],
+            "clocks": rec["clocks"],
+            "timed_s": rec["timed_s"],
         }
+        if "verify" in rec:
+            line["verify"] = rec["verify"]
+        if subs is not None:
+            line["sub_records"] = subs
+        elif not single and world > 1:
+            line["sub_records"] = "measured at one GPU only"
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

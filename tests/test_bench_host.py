@@ -56,12 +56,12 @@ def test_clock_summary_uses_only_the_timed_window(bench):
                  (1.0, row(2070, *ok)), (1.2, row(2055, "Active", *ok[1:])),
                  (1.4, row(2040, *ok)),
                  (3.0, row(600, "Not Active", "Active", "Not Active", "Not Active"))]
-    s.t0, s.t1 = 1.0, 2.0
-    c = s.summary()
+    c = s.summary(1.0, 2.0)
     assert c["sm_mhz"] == 2055 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
     assert c["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample lies after the window
-    s.t0, s.t1 = 5.0, 6.0
-    assert s.summary()["reasons"] == ["no samples"]
+    assert s.summary(5.0, 6.0)["reasons"] == ["no samples"]
+    # each record of a run summarises its own window
+    assert s.summary(2.5, 3.5)["reasons"] == ["hw_slowdown"]
 
 
 def test_ncu_traffic_needs_the_profiled_sources(bench, monkeypatch):
@@ -80,3 +80,23 @@ def test_ncu_traffic_needs_the_profiled_sources(bench, monkeypatch):
 def test_job_throughput_counts_every_rank(bench):
     # tokens of all ranks over the slowest rank's time
     assert bench.job_tokens_per_s(4, 256, 10, 500.0) == pytest.approx(4 * 256 * 10 / 0.5)
+
+
+def test_verify_union_bytes(bench):
+    """A verify call streams its distinct experts and the shared one once:
+    14.5 experts on average give (14.5 + 1) x 21,233,664 B of experts plus the
+    router (256 x 6144 fp32 weights and 256 biases), 4 rows of x and y."""
+    from workloads import CONFIGS
+    wl = CONFIGS["glm_verify"]
+    per_expert = 21_233_664
+    router = 256 * 6144 * 4 + 256 * 4
+    want = 15.5 * per_expert + router + 4 * 6144 * 2 + 4 * 6144 * 4
+    assert bench.union_bytes_per_call(wl, 14.5, 2) == pytest.approx(want)
+    # the accepted-token rates of the MTP A/B the per-emitted-token figures use
+    assert dict(bench.ACCEPTED_PER_VERIFY) == {"G4": 2.065, "G5": 2.286}
+
+
+def test_host_cpu_is_described(bench):
+    n, model = bench.host_cpu()
+    assert n == os.cpu_count() and n >= 1
+    assert isinstance(model, str) and model
