@@ -39,7 +39,18 @@ class _Layer(C.Structure):
         ("sh_gate_q", _u8p), ("sh_gate_s", _u16p),
         ("sh_up_q", _u8p), ("sh_up_s", _u16p),
         ("sh_down_q", _u8p), ("sh_down_s", _u16p),
+        ("wfmt", C.c_int), ("gsz", C.c_int),
     ]
+
+
+# weight formats of the oracle (R22)
+FMT_INT4, FMT_INT8 = 0, 1
+
+
+def shape_format(shape) -> tuple[int, int]:
+    """(fmt, gsz) of a layer shape: its weight format and scale group."""
+    fmt = FMT_INT8 if getattr(shape, "weight_format", "int4") == "int8" else FMT_INT4
+    return fmt, int(getattr(shape, "group_size", 32))
 
 
 def lib():
@@ -63,6 +74,10 @@ def lib():
         L.oracle_rmsnorm.argtypes = [_f32p, C.c_int, C.c_int, _f32p, C.c_double, _f32p]
         L.oracle_expert.argtypes = [_f32p, C.c_int, C.c_int, _u8p, _u16p, _u8p, _u16p,
                                     _u8p, _u16p, C.c_int, _f64p]
+        L.oracle_dequant_fmt.restype = C.c_float
+        L.oracle_dequant_fmt.argtypes = [_u8p, _u16p, C.c_int, C.c_int, C.c_int]
+        L.oracle_expert_fmt.argtypes = [_f32p, C.c_int, C.c_int, C.c_int, C.c_int, _u8p, _u16p,
+                                        _u8p, _u16p, _u8p, _u16p, C.c_int, _f64p]
         L.oracle_moe_forward.argtypes = [C.POINTER(_Layer), _f32p, C.c_int, C.c_double,
                                          _f32p, _f32p, C.c_int, _i32p, _f32p, _f32p, _f32p]
         _lib = L
@@ -93,6 +108,13 @@ def dequant(row_q: np.ndarray, row_s: np.ndarray, k: int) -> float:
     row_q = np.ascontiguousarray(row_q, dtype=np.uint8)
     row_s = np.ascontiguousarray(row_s, dtype=np.uint16)
     return float(lib().oracle_dequant(_p(row_q, _u8p), _p(row_s, _u16p), k))
+
+
+def dequant_fmt(row_q: np.ndarray, row_s: np.ndarray, k: int, fmt: int, gsz: int) -> float:
+    """Element k of one row in weight format fmt and scale group gsz (R22)."""
+    row_q = np.ascontiguousarray(row_q, dtype=np.uint8)
+    row_s = np.ascontiguousarray(row_s, dtype=np.uint16)
+    return float(lib().oracle_dequant_fmt(_p(row_q, _u8p), _p(row_s, _u16p), k, fmt, gsz))
 
 
 def router_logits(x: np.ndarray, Wr: np.ndarray) -> np.ndarray:
@@ -159,6 +181,21 @@ def expert(x: np.ndarray, inter: int, mats, prec: int = 0) -> np.ndarray:
     return out
 
 
+def expert_fmt(x: np.ndarray, inter: int, mats, fmt: int, gsz: int,
+               prec: int = 0) -> np.ndarray:
+    """One expert of weight format fmt and scale group gsz (R22) on one token."""
+    x = _f32(x).reshape(-1)
+    H = x.shape[0]
+    gq, gs, uq, us, dq, ds = [np.ascontiguousarray(m) for m in mats]
+    out = np.empty(H, np.float64)
+    rc = lib().oracle_expert_fmt(_p(x, _f32p), H, inter, fmt, gsz, _p(gq, _u8p), _p(gs, _u16p),
+                                 _p(uq, _u8p), _p(us, _u16p), _p(dq, _u8p), _p(ds, _u16p),
+                                 prec, _p(out, _f64p))
+    if rc:
+        raise ValueError("oracle_expert_fmt: bad shape or format")
+    return out
+
+
 def route(shape, router_w, router_b, x, eps: float = 0.0, gamma=None):
     """(x_hat, logits, ids, w) for activations x [T, H] (fp32 view)."""
     x = _f32(x)
@@ -193,6 +230,7 @@ def moe_forward(shape, router_w, router_b, get_expert, shared, x, eps: float = 0
     L = _Layer()
     L.hidden, L.inter, L.n_experts, L.top_k = H, shape.inter, E, shape.top_k
     L.n_group, L.topk_group, L.rsf = shape.n_group, shape.topk_group, shape.routed_scaling_factor
+    L.wfmt, L.gsz = shape_format(shape)
     L.router_w, L.router_b = _p(rw, _f32p), _p(rb, _f32p)
     L.gate_q, L.gate_s, L.up_q, L.up_s, L.down_q, L.down_s = tabs
     if shared is not None and shape.n_shared > 0:
@@ -219,5 +257,6 @@ def moe_forward(shape, router_w, router_b, get_expert, shared, x, eps: float = 0
     return y, ids, w, lg
 
 
-__all__ = ["router_exp", "router_sigmoid", "half_to_float", "dequant", "router_logits",
-           "select", "plan", "rmsnorm", "expert", "route", "moe_forward", "lib"]
+__all__ = ["router_exp", "router_sigmoid", "half_to_float", "dequant", "dequant_fmt",
+           "router_logits", "select", "plan", "rmsnorm", "expert", "expert_fmt", "route",
+           "moe_forward", "shape_format", "FMT_INT4", "FMT_INT8", "lib"]

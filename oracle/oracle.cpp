@@ -45,6 +45,12 @@
 //   R13 RMSNorm: fixed fp64 sum order stated at rmsnorm_row(); the
 //       reciprocal root is rounded to fp32 and applied with fp32 products;
 //       gamma is multiplicative; normalised activations stay fp32.
+//   R22 the other expert formats ([P1] N2: symmetric int4/int8, per-row or
+//       grouped scales; G2 status: Q8 applies its scale to the signed
+//       two's-complement byte, and a whole-row scale repeated over 32-value
+//       groups leaves every dequantised value unchanged): int8 weights one
+//       signed byte per element, K bytes per row; per-row scales one fp16 per
+//       row.  Stated at dequant_fmt().
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC.
 // Contraction must stay off: every fused multiply-add below is written as
@@ -87,13 +93,36 @@ float half_to_float(uint16_t h) {
   return sign ? -mag : mag;
 }
 
+// The stored code u of element k of a packed int4 row (R7 nibble order).
+int int4_code(const uint8_t* row_q, int k) {
+  const uint8_t byte = row_q[k >> 1];
+  return (k & 1) ? (byte >> 4) : (byte & 0xF);
+}
+
 // Dequantised weight: (u - 8) * scale, exact in fp32 ([P1] G2 status:
 // offset-binary, bias = -8 * scale).  Nibble order R7.
 float dequant(const uint8_t* row_q, const uint16_t* row_s, int k) {
-  const uint8_t byte = row_q[k >> 1];
-  const int u = (k & 1) ? (byte >> 4) : (byte & 0xF);
+  const int u = int4_code(row_q, k);
   const float s = half_to_float(row_s[k / 32]);
   return (float)(u - 8) * s;
+}
+
+// Dequantised weight of the other formats (R22): element k of a K-long row
+// with weight format fmt (0: packed offset-binary int4 as in dequant(), 1:
+// signed int8, one byte per element) and scale group gsz (32: one fp16 scale
+// per 32 elements; 0: one fp16 scale for the whole row).  Exact in fp32: q
+// has at most 8 significant bits and the scale 11.
+float dequant_fmt(const uint8_t* row_q, const uint16_t* row_s, int k, int fmt, int gsz) {
+  if (fmt == 0 && gsz == 32) return dequant(row_q, row_s, k);
+  int q;
+  if (fmt == 1) {
+    const uint8_t byte = row_q[k];
+    q = byte < 128 ? (int)byte : (int)byte - 256;  // two's complement
+  } else {
+    q = int4_code(row_q, k) - 8;
+  }
+  const float s = half_to_float(row_s[gsz == 0 ? 0 : k / gsz]);
+  return (float)q * s;
 }
 
 // ------------------------------------------------------------------ router --
@@ -343,50 +372,71 @@ namespace {
 //   g_i = sum_k Wg[i,k] x_k,  u_i = sum_k Wu[i,k] x_k        (k ascending)
 //   h_i = silu(g_i) * u_i,    silu(z) = z / (1 + exp(-z))
 //   o_r = sum_i Wd[r,i] h_i                                   (i ascending)
+// Weight format fmt and scale group gsz as in dequant_fmt() (R22): a row
+// holds K / 2 (int4) or K (int8) bytes and K / 32 or 1 scales.
 template <typename Acc>
-void expert_swiglu(const float* x, int H, int I, const uint8_t* gq,
+void expert_swiglu(const float* x, int H, int I, int fmt, int gsz, const uint8_t* gq,
                    const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
                    const uint8_t* dq, const uint16_t* ds, Acc* out) {
+  const size_t qh = fmt == 1 ? (size_t)H : (size_t)H / 2;
+  const size_t qi = fmt == 1 ? (size_t)I : (size_t)I / 2;
+  const size_t sh = gsz == 0 ? 1 : (size_t)H / 32;
+  const size_t si = gsz == 0 ? 1 : (size_t)I / 32;
   std::vector<Acc> h(I);
   for (int i = 0; i < I; ++i) {
-    const uint8_t* gr = gq + (size_t)i * (H / 2);
-    const uint16_t* gsr = gs + (size_t)i * (H / 32);
-    const uint8_t* ur = uq + (size_t)i * (H / 2);
-    const uint16_t* usr = us + (size_t)i * (H / 32);
+    const uint8_t* gr = gq + (size_t)i * qh;
+    const uint16_t* gsr = gs + (size_t)i * sh;
+    const uint8_t* ur = uq + (size_t)i * qh;
+    const uint16_t* usr = us + (size_t)i * sh;
     Acc g = 0, u = 0;
     for (int k = 0; k < H; ++k) {
-      g = g + (Acc)dequant(gr, gsr, k) * (Acc)x[k];
-      u = u + (Acc)dequant(ur, usr, k) * (Acc)x[k];
+      g = g + (Acc)dequant_fmt(gr, gsr, k, fmt, gsz) * (Acc)x[k];
+      u = u + (Acc)dequant_fmt(ur, usr, k, fmt, gsz) * (Acc)x[k];
     }
     const Acc silu = g / ((Acc)1 + std::exp(-g));
     h[i] = silu * u;
   }
   for (int r = 0; r < H; ++r) {
-    const uint8_t* dr = dq + (size_t)r * (I / 2);
-    const uint16_t* dsr = ds + (size_t)r * (I / 32);
+    const uint8_t* dr = dq + (size_t)r * qi;
+    const uint16_t* dsr = ds + (size_t)r * si;
     Acc o = 0;
-    for (int i = 0; i < I; ++i) o = o + (Acc)dequant(dr, dsr, i) * h[i];
+    for (int i = 0; i < I; ++i) o = o + (Acc)dequant_fmt(dr, dsr, i, fmt, gsz) * h[i];
     out[r] = o;
   }
 }
+
+bool fmt_ok(int fmt, int gsz) { return (fmt == 0 || fmt == 1) && (gsz == 32 || gsz == 0); }
 
 }  // namespace
 
 extern "C" {
 
-// One expert on one token, fp32 (prec=0) or fp64 (prec=1) accumulation.
+float oracle_dequant_fmt(const uint8_t* row_q, const uint16_t* row_s, int k, int fmt,
+                         int gsz) {
+  return dequant_fmt(row_q, row_s, k, fmt, gsz);
+}
+
+// One expert of any format (R22) on one token, fp32 (prec=0) or fp64 (prec=1).
+int oracle_expert_fmt(const float* x, int H, int I, int fmt, int gsz, const uint8_t* gq,
+                      const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
+                      const uint8_t* dq, const uint16_t* ds, int prec, double* out) {
+  if (H % 32 != 0 || I % 32 != 0 || !fmt_ok(fmt, gsz)) return -1;
+  if (prec == 0) {
+    std::vector<float> o(H);
+    expert_swiglu<float>(x, H, I, fmt, gsz, gq, gs, uq, us, dq, ds, o.data());
+    for (int r = 0; r < H; ++r) out[r] = o[r];
+  } else {
+    expert_swiglu<double>(x, H, I, fmt, gsz, gq, gs, uq, us, dq, ds, out);
+  }
+  return 0;
+}
+
+// One grouped-int4 expert on one token, fp32 (prec=0) or fp64 (prec=1)
+// accumulation.
 int oracle_expert(const float* x, int H, int I, const uint8_t* gq,
                   const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
                   const uint8_t* dq, const uint16_t* ds, int prec, double* out) {
-  if (H % 32 != 0 || I % 32 != 0) return -1;
-  if (prec == 0) {
-    std::vector<float> o(H);
-    expert_swiglu<float>(x, H, I, gq, gs, uq, us, dq, ds, o.data());
-    for (int r = 0; r < H; ++r) out[r] = o[r];
-  } else {
-    expert_swiglu<double>(x, H, I, gq, gs, uq, us, dq, ds, out);
-  }
-  return 0;
+  return oracle_expert_fmt(x, H, I, 0, 32, gq, gs, uq, us, dq, ds, prec, out);
 }
 
 struct oracle_layer {
@@ -408,7 +458,16 @@ struct oracle_layer {
   const uint16_t* sh_up_s;
   const uint8_t* sh_down_q;
   const uint16_t* sh_down_s;
+  int wfmt;  // weight format of every expert (R22): 0 int4, 1 int8
+  int gsz;   // scale group: 32, or 0 for one scale per row
 };
+
+// One expert of the layer's format.
+static int layer_expert(const oracle_layer* L, const float* x, int I, const uint8_t* gq,
+                 const uint16_t* gs, const uint8_t* uq, const uint16_t* us, const uint8_t* dq,
+                 const uint16_t* ds, int prec, double* out) {
+  return oracle_expert_fmt(x, L->hidden, I, L->wfmt, L->gsz, gq, gs, uq, us, dq, ds, prec, out);
+}
 
 // Whole layer on T tokens ([P1] N1 MoE bullet, N4, G2 status; [P3]).
 //   x_hat = rmsnorm(x) when gamma_or_null/eps given (eps > 0), else x
@@ -444,8 +503,9 @@ int oracle_moe_forward(const oracle_layer* L, const float* x, int T, double eps,
       if (!L->gate_q[e] || !L->gate_s[e] || !L->up_q[e] || !L->up_s[e] ||
           !L->down_q[e] || !L->down_s[e])
         return -3;  // caller did not supply a selected expert
-      oracle_expert(xt, H, L->inter, L->gate_q[e], L->gate_s[e], L->up_q[e],
-                    L->up_s[e], L->down_q[e], L->down_s[e], prec, o.data());
+      if (layer_expert(L, xt, L->inter, L->gate_q[e], L->gate_s[e], L->up_q[e], L->up_s[e],
+                       L->down_q[e], L->down_s[e], prec, o.data()))
+        return -4;
       for (int r = 0; r < H; ++r) {
         if (prec == 0)
           accf[r] = accf[r] + wj * (float)o[r];
@@ -454,8 +514,9 @@ int oracle_moe_forward(const oracle_layer* L, const float* x, int T, double eps,
       }
     }
     if (L->n_shared > 0) {
-      oracle_expert(xt, H, L->shared_inter, L->sh_gate_q, L->sh_gate_s, L->sh_up_q,
-                    L->sh_up_s, L->sh_down_q, L->sh_down_s, prec, o.data());
+      if (layer_expert(L, xt, L->shared_inter, L->sh_gate_q, L->sh_gate_s, L->sh_up_q,
+                       L->sh_up_s, L->sh_down_q, L->sh_down_s, prec, o.data()))
+        return -4;
       for (int r = 0; r < H; ++r) {
         if (prec == 0)
           accf[r] = accf[r] + (float)o[r];

@@ -3,8 +3,8 @@
 Each mutant changes one place of a copy of oracle/oracle.cpp the way a slip
 would: a wrong sign, index or constant, a dropped term, swapped operands, the
 wrong tie rule, a plan in the wrong order.  The copy is compiled with the
-oracle's own flags under oracle/_build/mutants/, and tests/test_oracle_pins.py
-runs against it in a subprocess (MOE_ORACLE_LIB names the build); that run must
+oracle's own flags under oracle/_build/mutants/, and tests/test_oracle_pins.py and
+tests/test_oracle_formats.py run against it in a subprocess (MOE_ORACLE_LIB names the build); that run must
 fail.  The unaltered source, built and run the same way, must pass, so that each
 failure is the slip's doing and not the harness's.  Everything happens on the
 CPU; the CUDA library is not involved.
@@ -21,7 +21,8 @@ import pytest
 from oracle import build as oracle_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+PINS = [os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+        os.path.join(ROOT, "tests", "test_oracle_formats.py")]
 OUT = os.path.join(ROOT, "oracle", "_build", "mutants")
 
 # name -> (text in oracle.cpp, exactly once; its replacement)
@@ -76,8 +77,9 @@ MUTANTS = {
     "swiglu_gate_and_up_swapped": (
         "const Acc silu = g / ((Acc)1 + std::exp(-g));\n    h[i] = silu * u;",
         "const Acc silu = u / ((Acc)1 + std::exp(-u));\n    h[i] = silu * g;"),
-    "up_with_gate_scales": ("u = u + (Acc)dequant(ur, usr, k)", "u = u + (Acc)dequant(ur, gsr, k)"),
-    "down_scale_row_stride": ("ds + (size_t)r * (I / 32)", "ds + (size_t)r * (I / 64)"),
+    "up_with_gate_scales": ("u = u + (Acc)dequant_fmt(ur, usr, k", "u = u + (Acc)dequant_fmt(ur, gsr, k"),
+    "down_scale_row_stride": ("const size_t si = gsz == 0 ? 1 : (size_t)I / 32;",
+                              "const size_t si = gsz == 0 ? 1 : (size_t)I / 64;"),
     # layer combine
     "routed_weight_dropped": ("accf[r] = accf[r] + wj * (float)o[r];",
                               "accf[r] = accf[r] + (float)o[r];"),
@@ -99,6 +101,16 @@ MUTANTS = {
                             "for (int i = 0; i + 1 < I; ++i) o = o"),
     "layer_rows_read_token_0": ("const float* xt = xh.data() + (size_t)t * H;",
                                 "const float* xt = xh.data();"),
+    # the other expert formats (int8, one scale per row)
+    "int8_read_unsigned": ("q = byte < 128 ? (int)byte : (int)byte - 256;", "q = (int)byte;"),
+    "int8_offset_binary": ("q = byte < 128 ? (int)byte : (int)byte - 256;",
+                           "q = (int)byte - 128;"),
+    "int8_rows_at_int4_stride": ("const size_t qh = fmt == 1 ? (size_t)H : (size_t)H / 2;",
+                                 "const size_t qh = (size_t)H / 2;"),
+    "row_scales_of_row_0": ("const size_t sh = gsz == 0 ? 1 : (size_t)H / 32;",
+                            "const size_t sh = gsz == 0 ? 0 : (size_t)H / 32;"),
+    "row_scale_int4_offset_7": ("q = int4_code(row_q, k) - 8;", "q = int4_code(row_q, k) - 7;"),
+    "layer_scale_group_dropped": ("L->wfmt, L->gsz, gq", "L->wfmt, 0, gq"),
 }
 
 
@@ -115,7 +127,7 @@ def _run_pins(name: str, text: str) -> tuple[str, int, str]:
         f.write(text)
     oracle_build.compile_source(src, lib)
     env = dict(os.environ, MOE_ORACLE_LIB=lib)
-    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider",
+    r = subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-p", "no:cacheprovider",
                         "-m", "not gpu"], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=600)
     return name, r.returncode, (r.stdout + r.stderr)[-600:]

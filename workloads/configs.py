@@ -31,22 +31,27 @@ class LayerShape:
     routed_scaling_factor: float
     n_shared: int = 1
     shared_inter: int = 0  # 0 -> same as inter
-    group_size: int = 32
+    group_size: int = 32   # 32, or 0 for one fp16 scale per row
+    weight_format: str = "int4"  # "int4" (offset-binary nibbles) or "int8" (signed bytes)
 
     @property
     def i_shared(self) -> int:
         return self.shared_inter or self.inter
 
+    def matrix_bytes(self, rows: int, cols: int) -> int:
+        """Weights and fp16 scales of one rows x cols matrix in this format."""
+        q = rows * cols if self.weight_format == "int8" else rows * cols // 2
+        n_sc = rows if self.group_size == 0 else rows * (cols // self.group_size)
+        return q + 2 * n_sc
+
     def expert_bytes(self) -> int:
-        """Packed nibbles + fp16 group scales of one routed expert."""
-        h, i, g = self.hidden, self.inter, self.group_size
-        packed = 3 * h * i // 2
-        scales = 2 * (i * h // g) * 2 + (h * i // g) * 2
-        return packed + scales
+        """Weights + scales of one routed expert (gate, up, down)."""
+        h, i = self.hidden, self.inter
+        return 2 * self.matrix_bytes(i, h) + self.matrix_bytes(h, i)
 
     def shared_bytes(self) -> int:
-        h, i, g = self.hidden, self.i_shared, self.group_size
-        return 3 * h * i // 2 + 3 * (h * i // g) * 2
+        h, i = self.hidden, self.i_shared
+        return 2 * self.matrix_bytes(i, h) + self.matrix_bytes(h, i)
 
     def router_bytes(self) -> int:
         return self.n_experts * self.hidden * 4 + self.n_experts * 4

@@ -86,22 +86,31 @@ def _scale_table_t(device) -> torch.Tensor:
 
 
 def gen_expert_matrix(seed: int, layer: int, mat: int, experts, rows: int,
-                      cols: int, device="cpu", group_size: int = 32):
-    """Packed nibbles [n, rows, cols/2] uint8 and scales [n, rows, cols/g] fp16.
+                      cols: int, device="cpu", group_size: int = 32, fmt: str = "int4"):
+    """Weights and fp16 scales of one matrix per listed expert.
 
-    ``experts`` lists expert indices (``SHARED_EXPERT`` = -1 for the shared
-    expert).  Row-major, K (= cols) contiguous.  Each output row is
-    independent of which other experts are generated in the same call.
+    int4: packed nibbles [n, rows, cols/2] uint8; int8: signed bytes [n, rows,
+    cols] (stored as uint8, uniform over all 256 codes).  Scales [n, rows,
+    cols/g] for group size g, or [n, rows, 1] for group_size 0 (one scale a
+    row).  int8 scales are the int4 table divided by 16 (exact in fp16), so
+    the weights span about the same range in both formats.  ``experts``
+    lists expert indices (``SHARED_EXPERT`` = -1 for the shared expert).
+    Row-major, K (= cols) contiguous.  Each output row is independent of
+    which other experts are generated in the same call.
     """
     experts = torch.as_tensor(experts, dtype=torch.int64)
     n = experts.numel()
-    assert cols % 8 == 0 and cols % group_size == 0
-    n_words = rows * cols // 8
+    assert cols % 8 == 0 and (group_size == 0 or cols % group_size == 0)
+    bpr = cols if fmt == "int8" else cols // 2  # weight bytes a row
+    n_words = rows * bpr // 4
     q = _to_u32_bytes(_words(seed, layer, mat, experts, n_words, device, 0x1B873593))
-    q = q.view(n, rows, cols // 2)
-    n_sc = rows * (cols // group_size)
-    sidx = _words(seed, layer, mat, experts, n_sc, device, 0x3C6EF372) & 1023
-    s = _scale_table_t(device)[sidx].view(n, rows, cols // group_size)
+    q = q.view(n, rows, bpr)
+    spr = 1 if group_size == 0 else cols // group_size  # scales a row
+    sidx = _words(seed, layer, mat, experts, rows * spr, device, 0x3C6EF372) & 1023
+    table = _scale_table_t(device)
+    if fmt == "int8":
+        table = table / 16
+    s = table[sidx].view(n, rows, spr)
     return q, s
 
 
@@ -174,12 +183,14 @@ class LayerInputs:
     sh_down_s: torch.Tensor
 
 
-def _gen_mat_all(seed, layer, mat, E, rows, cols, device, chunk):
-    q = torch.empty(E, rows, cols // 2, dtype=torch.uint8, device=device)
-    s = torch.empty(E, rows, cols // 32, dtype=torch.float16, device=device)
+def _gen_mat_all(seed, layer, mat, E, rows, cols, device, chunk, group_size=32, fmt="int4"):
+    bpr = cols if fmt == "int8" else cols // 2
+    spr = 1 if group_size == 0 else cols // group_size
+    q = torch.empty(E, rows, bpr, dtype=torch.uint8, device=device)
+    s = torch.empty(E, rows, spr, dtype=torch.float16, device=device)
     for e0 in range(0, E, chunk):
         ex = list(range(e0, min(E, e0 + chunk)))
-        qq, ss = gen_expert_matrix(seed, layer, mat, ex, rows, cols, device)
+        qq, ss = gen_expert_matrix(seed, layer, mat, ex, rows, cols, device, group_size, fmt)
         q[e0:e0 + len(ex)] = qq
         s[e0:e0 + len(ex)] = ss
         del qq, ss
@@ -195,12 +206,13 @@ def gen_layer(w: Workload, layer: int = 0, device="cpu", chunk: int | None = Non
     if chunk is None:
         chunk = max(1, (1 << 25) // max(1, I * H // 8))
     rw, rb = gen_router(sh, seed, layer, w.bias_kind, w.zipf_s, zipf_kappa)
-    gq, gs = _gen_mat_all(seed, layer, GATE, E, I, H, device, chunk)
-    uq, us = _gen_mat_all(seed, layer, UP, E, I, H, device, chunk)
-    dq, ds = _gen_mat_all(seed, layer, DOWN, E, H, I, device, chunk)
-    sgq, sgs = gen_expert_matrix(seed, layer, GATE, [SHARED_EXPERT], Is, H, device)
-    suq, sus = gen_expert_matrix(seed, layer, UP, [SHARED_EXPERT], Is, H, device)
-    sdq, sds = gen_expert_matrix(seed, layer, DOWN, [SHARED_EXPERT], H, Is, device)
+    f = (sh.group_size, sh.weight_format)
+    gq, gs = _gen_mat_all(seed, layer, GATE, E, I, H, device, chunk, *f)
+    uq, us = _gen_mat_all(seed, layer, UP, E, I, H, device, chunk, *f)
+    dq, ds = _gen_mat_all(seed, layer, DOWN, E, H, I, device, chunk, *f)
+    sgq, sgs = gen_expert_matrix(seed, layer, GATE, [SHARED_EXPERT], Is, H, device, *f)
+    suq, sus = gen_expert_matrix(seed, layer, UP, [SHARED_EXPERT], Is, H, device, *f)
+    sdq, sds = gen_expert_matrix(seed, layer, DOWN, [SHARED_EXPERT], H, Is, device, *f)
     return LayerInputs(sh, rw.to(device), rb.to(device), gq, gs, uq, us, dq, ds,
                        sgq[0].contiguous(), sgs[0].contiguous(), suq[0].contiguous(),
                        sus[0].contiguous(), sdq[0].contiguous(), sds[0].contiguous())
@@ -227,7 +239,8 @@ class HostExpertCache:
             I = sh.i_shared if e == SHARED_EXPERT else sh.inter
             out = []
             for mat, (r, c) in ((GATE, (I, H)), (UP, (I, H)), (DOWN, (H, I))):
-                q, s = gen_expert_matrix(self.seed, self.layer, mat, [e], r, c, "cpu")
+                q, s = gen_expert_matrix(self.seed, self.layer, mat, [e], r, c, "cpu",
+                                         sh.group_size, sh.weight_format)
                 out.append(np.ascontiguousarray(q[0].numpy()))
                 out.append(np.ascontiguousarray(s[0].view(torch.int16).numpy().view(np.uint16)))
             self._cache[e] = tuple(out)
