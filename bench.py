@@ -16,9 +16,9 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU
 `--impl reference` times the CPU oracle (the reference arm) on rank 0.
 
 Without --workload the run measures glm_decode (the headline line) and then,
-at one GPU, glm_verify, glm_prefill, glm_stack and glm_prefill_uniform as
-sub-records of the same line, each timed for at least 1.5 s with its own
-clock record.
+at one GPU, glm_verify, glm_prefill, glm_stack, glm_prefill_uniform and
+glm_decode_rowscale (one scale a row) as sub-records of the same line, each
+timed for at least 1.5 s with its own clock record.
 """
 from __future__ import annotations
 
@@ -194,12 +194,12 @@ def ncu_traffic(kernel: str, workload: str):
 # ----------------------------------------------------- algorithmic bytes ----
 
 def expert_gate_up_bytes(sh):
-    return 2 * (sh.inter * sh.hidden // 2 + sh.inter * sh.hidden // 32 * 2)
+    """Gate and up weights with their scales, in the shape's format."""
+    return 2 * sh.matrix_bytes(sh.inter, sh.hidden)
 
 
 def expert_down_bytes(sh, inter=None):
-    I = inter or sh.inter
-    return sh.hidden * I // 2 + sh.hidden * I // 32 * 2
+    return sh.matrix_bytes(sh.hidden, inter or sh.inter)
 
 
 def phase_bytes(phase, sh, T, n_act, x_bytes):
@@ -472,7 +472,8 @@ def run_reference(args, wl):
 
 # The workloads the default run measures after the headline (one process, one
 # after another, each layer stack freed before the next is generated).
-SUB_WORKLOADS = ("glm_verify", "glm_prefill", "glm_stack", "glm_prefill_uniform")
+SUB_WORKLOADS = ("glm_verify", "glm_prefill", "glm_stack", "glm_prefill_uniform",
+                 "glm_decode_rowscale")
 # A sub-record's timed region lasts at least this long, so that the 200 ms
 # clock sampler sees several samples under load.
 SUB_MIN_TIMED_S = 1.5
@@ -665,7 +666,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
-                             "glm_prefill_uniform"],
+                             "glm_prefill_uniform", "glm_decode_rowscale"],
                     help="one workload only (default: glm_decode, then the other GLM "
                          "workloads as sub-records)")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")

@@ -73,13 +73,27 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
+/* Expert weight formats ("GLM-5.2 on a 32 GB Mac", N2: symmetric int4/int8
+ * with per-row or grouped scales; "G2 implementation status": offset-binary
+ * Q4 with bias -8 * scale, Q8 scaling the signed two's-complement byte).
+ *   MOE_W_INT4: two elements a byte, element 2j in the low nibble of byte j,
+ *               value (u - 8) * scale for the stored code u.
+ *   MOE_W_INT8: one signed two's-complement byte an element, value
+ *               q * scale. */
+typedef enum { MOE_W_INT4 = 0, MOE_W_INT8 = 1 } moe_wformat_t;
+
 /* Layer geometry.  Requirements (else MOE_ERR_UNSUPPORTED):
  *   hidden % 256 == 0 and 256 <= hidden <= 12288;
  *   inter % 32 == 0, shared_inter % 32 == 0 (if n_shared), both <= 8192;
  *   1 <= n_experts <= 1024, n_experts % n_group == 0;
  *   1 <= topk_group <= n_group, 1 <= top_k <= 32,
  *   top_k <= topk_group * (n_experts / n_group);
- *   group_size == 32; n_shared in {0, 1}; 1 <= max_tokens <= 65536. */
+ *   group_size 32 or 0; weight_format MOE_W_INT4 or MOE_W_INT8;
+ *   n_shared in {0, 1}; 1 <= max_tokens <= 65536.
+ * The tensor-core paths (grouped GEMM, single-token tensor-core kernel) take
+ * grouped int4 only; a handle of another format runs T = 1 on the
+ * single-token SIMT kernel (per-row int4) or the SIMT batch path, and
+ * T > 1 on the SIMT batch path. */
 typedef struct {
   int hidden;                  /* H */
   int inter;                   /* I, routed expert intermediate size */
@@ -90,12 +104,16 @@ typedef struct {
   float routed_scaling_factor; /* multiplies the renormalised gate weights */
   int n_shared;                /* 0 or 1 always-on shared expert */
   int shared_inter;            /* shared expert intermediate size */
-  int group_size;              /* quantisation group along K; must be 32 */
+  int group_size;              /* fp16 scales along K: one per 32 values (32) or one
+                                  per row (0, Colibri's whole-row group) */
   int max_tokens;              /* largest T any call on this handle may pass */
+  int weight_format;           /* moe_wformat_t of every expert matrix */
 } moe_config_t;
 
 /* Device pointers, borrowed for the handle's lifetime.  Every pointer must
- * be 16-byte aligned.  sh_* may be NULL when n_shared == 0. */
+ * be 16-byte aligned.  sh_* may be NULL when n_shared == 0.  Shapes for
+ * MOE_W_INT4 with group_size 32; a MOE_W_INT8 row holds K bytes instead of
+ * K/2, and with group_size 0 a row has one scale instead of K/32. */
 typedef struct {
   const float* router_w;    /* [E][H] fp32 */
   const float* router_bias; /* [E] fp32 score-correction bias */

@@ -46,7 +46,10 @@ const char* check_config(const moe_config_t* c) {
   if (c->top_k < 1 || c->top_k > 32) return "top_k must be in [1, 32]";
   if (c->top_k > c->topk_group * (c->n_experts / c->n_group))
     return "top_k exceeds the experts of the kept groups";
-  if (c->group_size != 32) return "group_size must be 32";
+  if (c->group_size != 32 && c->group_size != 0)
+    return "group_size must be 32 (grouped scales) or 0 (one scale a row)";
+  if (c->weight_format != MOE_W_INT4 && c->weight_format != MOE_W_INT8)
+    return "weight_format must be MOE_W_INT4 or MOE_W_INT8";
   if (c->max_tokens < 1 || c->max_tokens > 65536) return "max_tokens must be in [1, 65536]";
   if (!(c->routed_scaling_factor == c->routed_scaling_factor) ||
       c->routed_scaling_factor > 3.0e38f || c->routed_scaling_factor < -3.0e38f)
@@ -127,6 +130,9 @@ const char* check_extent(const void* p, size_t bytes, int device) {
 const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, int device,
                                 const char** which) {
   const size_t E = c->n_experts, H = c->hidden, I = c->inter;
+  // bytes of a K-long row's weights and of its scales, in the format
+  auto qb = [&](size_t K) { return c->weight_format == MOE_W_INT8 ? K : K / 2; };
+  auto sb = [&](size_t K) { return (c->group_size == 0 ? 1 : K / 32) * 2; };
   struct A {
     const char* name;
     const void* p;
@@ -134,12 +140,12 @@ const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, i
   };
   const A routed[] = {{"router_w", w->router_w, E * H * 4},
                       {"router_bias", w->router_bias, E * 4},
-                      {"gate_q", w->gate_q, E * I * H / 2},
-                      {"gate_s", w->gate_s, E * I * (H / 32) * 2},
-                      {"up_q", w->up_q, E * I * H / 2},
-                      {"up_s", w->up_s, E * I * (H / 32) * 2},
-                      {"down_q", w->down_q, E * H * I / 2},
-                      {"down_s", w->down_s, E * H * (I / 32) * 2}};
+                      {"gate_q", w->gate_q, E * I * qb(H)},
+                      {"gate_s", w->gate_s, E * I * sb(H)},
+                      {"up_q", w->up_q, E * I * qb(H)},
+                      {"up_s", w->up_s, E * I * sb(H)},
+                      {"down_q", w->down_q, E * H * qb(I)},
+                      {"down_s", w->down_s, E * H * sb(I)}};
   for (const A& x : routed)
     if (const char* m = check_extent(x.p, x.bytes, device)) {
       *which = x.name;
@@ -147,12 +153,12 @@ const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, i
     }
   if (!c->n_shared) return nullptr;
   const size_t Is = c->shared_inter;
-  const A shared[] = {{"sh_gate_q", w->sh_gate_q, Is * H / 2},
-                      {"sh_gate_s", w->sh_gate_s, Is * (H / 32) * 2},
-                      {"sh_up_q", w->sh_up_q, Is * H / 2},
-                      {"sh_up_s", w->sh_up_s, Is * (H / 32) * 2},
-                      {"sh_down_q", w->sh_down_q, H * Is / 2},
-                      {"sh_down_s", w->sh_down_s, H * (Is / 32) * 2}};
+  const A shared[] = {{"sh_gate_q", w->sh_gate_q, Is * qb(H)},
+                      {"sh_gate_s", w->sh_gate_s, Is * sb(H)},
+                      {"sh_up_q", w->sh_up_q, Is * qb(H)},
+                      {"sh_up_s", w->sh_up_s, Is * sb(H)},
+                      {"sh_down_q", w->sh_down_q, H * qb(Is)},
+                      {"sh_down_s", w->sh_down_s, H * sb(Is)}};
   for (const A& x : shared)
     if (const char* m = check_extent(x.p, x.bytes, device)) {
       *which = x.name;
@@ -434,7 +440,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
   h->w = *w;
   h->sh = Shape{cfg->hidden, cfg->inter, cfg->n_shared ? cfg->shared_inter : 0,
                 cfg->n_experts, cfg->top_k, cfg->n_group, cfg->topk_group, cfg->n_shared,
-                cfg->routed_scaling_factor};
+                cfg->routed_scaling_factor, cfg->weight_format, cfg->group_size};
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount,
                                                    h->device);

@@ -21,6 +21,7 @@ constexpr size_t kSmemLimit = 227 * 1024 - 1024;  // per-CTA opt-in limit, minus
 bool decode_path_ok(const Shape& sh, int T, int n_sm) {
   using namespace dec;
   if (T != 1 || sh.k > kMaxEntries) return false;
+  if (sh.wfmt != MOE_W_INT4) return false;  // int4, grouped or one scale a row
   const int epl = fast_select_epl(sh);
   if (epl < 1 || epl > 8) return false;
   if (n_sm < 1 || (sh.E + n_sm - 1) / n_sm > kMaxLocalExperts) return false;

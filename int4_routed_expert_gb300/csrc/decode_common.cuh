@@ -144,6 +144,22 @@ __device__ inline bool gbar_wait(unsigned long long* p, unsigned long long targe
   return ok != 0;
 }
 
+// 4- and 8-byte global -> shared copies (cp.async, through L1) and the
+// arrive-on of an mbarrier once this thread's copies so far have landed
+// (the pending count is raised first, so the phase waits for them).
+__device__ __forceinline__ void cp_async_ca4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_ca8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ const void* align_down4(const void* p) {
+  return reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(3));
+}
+
 // Release store of a monotonic generation word (read with gbar_wait).
 __device__ __forceinline__ void publish_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -198,6 +198,9 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
   bool planned = false;
   int issued = 0, consumed = 0;
   const uint32_t ring_w = smem_u32(ring + static_cast<size_t>(warp) * STAGES * SB);
+  // scales: one per 32 values, or one per row (group size 0)
+  const bool row_scaled = sh.gsz == 0;
+  const size_t ssh = row_scaled ? 1 : H / 32, ssi = row_scaled ? 1 : I / 32;
   const uint32_t magic = kMagic;
 
   auto rgu_at = [&](int o, int& slot, int& row) {
@@ -226,8 +229,8 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       gu = true;
       q0p = a.w.sh_gate_q + r * (H / 2);
       q1p = a.w.sh_up_q + r * (H / 2);
-      s0p = a.w.sh_gate_s + r * (H / 32);
-      s1p = a.w.sh_up_s + r * (H / 32);
+      s0p = a.w.sh_gate_s + r * ssh;
+      s1p = a.w.sh_up_s + r * ssh;
     } else if (j < n_sgu + n_rgu) {
       int slot, r;
       rgu_at(j - n_sgu, slot, r);
@@ -235,8 +238,8 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       gu = true;
       q0p = a.w.gate_q + row * (H / 2);
       q1p = a.w.up_q + row * (H / 2);
-      s0p = a.w.gate_s + row * (H / 32);
-      s1p = a.w.up_s + row * (H / 32);
+      s0p = a.w.gate_s + row * ssh;
+      s1p = a.w.up_s + row * ssh;
     } else {
       int si, lr;
       dn_at(j - n_sgu - n_rgu, si, lr);
@@ -245,10 +248,10 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       if (si < n_act_k) {
         const size_t row = static_cast<size_t>(s_pe[si]) * H + r0;
         q0p = a.w.down_q + row * (I / 2);
-        s0p = a.w.down_s + row * (I / 32);
+        s0p = a.w.down_s + row * ssi;
       } else {
         q0p = a.w.sh_down_q + r0 * (I / 2);
-        s0p = a.w.sh_down_s + r0 * (I / 32);
+        s0p = a.w.sh_down_s + r0 * ssi;
       }
     }
     if (lane == 0) {
@@ -256,7 +259,26 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       const uint32_t dst = ring_w + st * SB;
       const uint32_t bar = bar0 + 8 * st;
       fence_proxy_async_smem();
-      if (gu) {
+      if (row_scaled) {
+        // one scale a row: too small for a bulk copy, so the 4-byte word
+        // holding it (gate/up rows) or the 4 rows' 8 bytes (down) come by
+        // cp.async, whose arrival the stage's phase also waits for (the
+        // arrive comes first, so the phase cannot complete without it)
+        if (gu) {
+          cp_async_ca4(dst + H, align_down4(s0p));
+          cp_async_ca4(dst + H + 4, align_down4(s1p));
+        } else {
+          cp_async_ca8(dst + kRowsC * (I / 2), s0p);
+        }
+        cp_async_mbar_arrive(bar);
+        mbar_arrive_expect_tx(bar, gu ? H : kRowsC * (I / 2));
+        if (gu) {
+          bulk_g2s(dst, q0p, H / 2, bar);
+          bulk_g2s(dst + H / 2, q1p, H / 2, bar);
+        } else {
+          bulk_g2s(dst, q0p, kRowsC * (I / 2), bar);
+        }
+      } else if (gu) {
         mbar_arrive_expect_tx(bar, H + H / 8);
         bulk_g2s(dst, q0p, H / 2, bar);
         bulk_g2s(dst + H / 2, q1p, H / 2, bar);
@@ -461,8 +483,11 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       }
       const uint4* gq4 = reinterpret_cast<const uint4*>(sb);
       const uint4* uq4 = reinterpret_cast<const uint4*>(sb + H / 2);
+      // grouped: scale g of the row; one a row: the half of the 4-byte word
+      // that holds this row's scale (rows 2m, 2m + 1 share a word)
       const uint16_t* gsc = reinterpret_cast<const uint16_t*>(sb + H);
-      const uint16_t* usc = reinterpret_cast<const uint16_t*>(sb + H + H / 16);
+      const uint16_t* usc = row_scaled ? gsc + 2 : reinterpret_cast<const uint16_t*>(sb + H + H / 16);
+      const int smask = row_scaled ? 0 : -1, soff = row_scaled ? (row & 1) : 0;
       float2 ga = make_float2(0.f, 0.f), ua = ga;
       // kept rolled: the body is what a cold instruction cache has to fetch
 #pragma unroll 1
@@ -470,7 +495,8 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
         const int g = c * 32 + lane;
         if (CPLH == 1 && g >= GKH) break;
         const uint4 qa = gq4[g], qb = uq4[g];
-        const float sa = half_bits_to_f32(gsc[g]), sbv = half_bits_to_f32(usc[g]);
+        const float sa = half_bits_to_f32(gsc[(g & smask) + soff]);
+        const float sbv = half_bits_to_f32(usc[(g & smask) + soff]);
         const float4* xg = xs4 + (c * 8) * 32 + lane;
         float2 da0 = make_float2(0.f, 0.f), da1 = da0, db0 = da0, db1 = da0;
 #pragma unroll
@@ -533,8 +559,8 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
 #pragma unroll
         for (int r = 0; r < kRowsC; ++r) {
           q[r] = reinterpret_cast<const uint4*>(sb + r * (I / 2))[g];
-          sc[r] = half_bits_to_f32(
-              reinterpret_cast<const uint16_t*>(sb + kRowsC * (I / 2) + r * (I / 16))[g]);
+          sc[r] = half_bits_to_f32(reinterpret_cast<const uint16_t*>(sb + kRowsC * (I / 2))
+                                       [row_scaled ? r : r * (I / 32) + g]);
         }
         float2 d0[kRowsC], d1[kRowsC];
 #pragma unroll

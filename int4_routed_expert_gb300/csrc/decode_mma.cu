@@ -170,15 +170,12 @@ __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t& a, uint32_t& b, u
                : "r"(addr));
 }
 
-// 16-byte global -> shared copy through L2 (cp.async), and the arrive-on of
-// an mbarrier once this thread's copies so far have landed (the pending
-// count is raised first, so the phase waits for them).
+// 16-byte global -> shared copy through L2 (cp.async); its mbarrier
+// arrive-on is dec::cp_async_mbar_arrive.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
+using dec::cp_async_mbar_arrive;
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -901,6 +898,7 @@ Plan plan_of(const Shape& sh, int G) {
 }  // namespace dm
 
 bool dm_shape_ok(const Shape& sh) {
+  if (!grouped_int4(sh)) return false;
   if (sh.H % dm::kKc != 0 || sh.H > 12288) return false;
   if (sh.I % dm::kKc != 0) return false;
   if (sh.n_shared && sh.Is != sh.I) return false;

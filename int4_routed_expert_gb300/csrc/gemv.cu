@@ -15,6 +15,10 @@
 // A CTA owns a tile of kNT consecutive plan positions (or kNT tokens of the
 // shared expert) and 64 output rows; positions of one expert inside the tile
 // form one run that streams each weight row once for all of its tokens.
+//
+// Every expert format runs here (N2: symmetric int4/int8, per-row or grouped
+// scales): packed offset-binary int4 or signed int8 weights, one fp16 scale
+// per 32 values or one per row.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -68,6 +72,45 @@ __device__ __forceinline__ void group_dot(const uint4 q, const float* xs, int ro
   }
 }
 
+// sum_{j<32} q_j * x_j for one group of 32 signed int8 weights (32 bytes,
+// element j in byte j: two's complement, "G2 implementation status" Q8).
+template <int NT>
+__device__ __forceinline__ void group_dot_i8(const uint4 q0, const uint4 q1, const float* xs,
+                                             int row_len, int g, float (&part)[NT]) {
+  const uint32_t wds[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int t = 0; t < NT; ++t) part[t] = 0.0f;
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) {
+    float qv[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+      qv[n] = static_cast<float>(static_cast<int8_t>((wds[wi] >> (8 * n)) & 0xFFu));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float4 a = *reinterpret_cast<const float4*>(xs + t * row_len + g * kGS + wi * 4);
+      float s = part[t];
+      s = fmaf(qv[0], a.x, s);
+      s = fmaf(qv[1], a.y, s);
+      s = fmaf(qv[2], a.z, s);
+      s = fmaf(qv[3], a.w, s);
+      part[t] = s;
+    }
+  }
+}
+
+// One group of a weight row in either format: int4 (16 bytes) or int8 (32).
+template <int FMT, int NT>
+__device__ __forceinline__ void group_dot_fmt(const uint8_t* row, const float* xs, int row_len,
+                                              int g, float (&part)[NT]) {
+  if (FMT == MOE_W_INT8) {
+    const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * g;
+    group_dot_i8<NT>(__ldg(q), __ldg(q + 1), xs, row_len, g, part);
+  } else {
+    group_dot<NT>(__ldg(reinterpret_cast<const uint4*>(row) + g), xs, row_len, g, part);
+  }
+}
+
 // Tile of the CTA: which rows of hbuf/obuf it produces, from which expert.
 struct Run {
   int e;       // expert (-1: shared)
@@ -109,28 +152,38 @@ __device__ inline int tile_runs(const Workspace& ws, int T, int k, int y, Run* r
   return nr;
 }
 
-template <int NT>
+// Row strides of a K-long row in the shape's format: weight bytes, scales,
+// and the scale index step per group (0: one scale for the whole row).
+struct RowFmt {
+  size_t qb, ns;
+  int sstep;
+};
+__device__ __forceinline__ RowFmt row_fmt(const Shape& sh, int K) {
+  return RowFmt{row_bytes(sh, K), row_scales(sh, K), sh.gsz == 0 ? 0 : 1};
+}
+
+template <int FMT, int NT>
 __device__ void gate_up_rows(const uint8_t* gq, const uint16_t* gs, const uint8_t* uq,
-                             const uint16_t* us, int H, int I, int r0, const float* xs,
-                             const Run& run, const Workspace& ws) {
+                             const uint16_t* us, int H, int I, const RowFmt& f, int r0,
+                             const float* xs, const Run& run, const Workspace& ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = H / 32, row_len = G * kGS;
   for (int rr = warp; rr < kRows; rr += kWarps) {
     const int r = r0 + rr;
     if (r >= I) break;
-    const uint4* gr = reinterpret_cast<const uint4*>(gq + static_cast<size_t>(r) * (H / 2));
-    const uint4* ur = reinterpret_cast<const uint4*>(uq + static_cast<size_t>(r) * (H / 2));
-    const uint16_t* gsr = gs + static_cast<size_t>(r) * G;
-    const uint16_t* usr = us + static_cast<size_t>(r) * G;
+    const uint8_t* gr = gq + static_cast<size_t>(r) * f.qb;
+    const uint8_t* ur = uq + static_cast<size_t>(r) * f.qb;
+    const uint16_t* gsr = gs + static_cast<size_t>(r) * f.ns;
+    const uint16_t* usr = us + static_cast<size_t>(r) * f.ns;
     float ga[NT], ua[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) ga[t] = ua[t] = 0.0f;
     for (int g = lane; g < G; g += 32) {
-      const uint4 a = __ldg(gr + g), b = __ldg(ur + g);
-      const float sa = half_to_f32(__ldg(gsr + g)), sb = half_to_f32(__ldg(usr + g));
+      const float sa = half_to_f32(__ldg(gsr + g * f.sstep));
+      const float sb = half_to_f32(__ldg(usr + g * f.sstep));
       float pa[NT], pb[NT];
-      group_dot<NT>(a, xs, row_len, g, pa);
-      group_dot<NT>(b, xs, row_len, g, pb);
+      group_dot_fmt<FMT, NT>(gr, xs, row_len, g, pa);
+      group_dot_fmt<FMT, NT>(ur, xs, row_len, g, pb);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         ga[t] = fmaf(sa, pa[t], ga[t]);
@@ -148,24 +201,23 @@ __device__ void gate_up_rows(const uint8_t* gq, const uint16_t* gs, const uint8_
   }
 }
 
-template <int NT>
-__device__ void down_rows(const uint8_t* dq, const uint16_t* ds, int H, int I, int r0,
-                          const float* hs, const Run& run, const Workspace& ws) {
+template <int FMT, int NT>
+__device__ void down_rows(const uint8_t* dq, const uint16_t* ds, int H, int I, const RowFmt& f,
+                          int r0, const float* hs, const Run& run, const Workspace& ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = I / 32, row_len = G * kGS;
   for (int rr = warp; rr < kRows; rr += kWarps) {
     const int r = r0 + rr;
     if (r >= H) break;
-    const uint4* dr = reinterpret_cast<const uint4*>(dq + static_cast<size_t>(r) * (I / 2));
-    const uint16_t* dsr = ds + static_cast<size_t>(r) * G;
+    const uint8_t* dr = dq + static_cast<size_t>(r) * f.qb;
+    const uint16_t* dsr = ds + static_cast<size_t>(r) * f.ns;
     float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
     for (int g = lane; g < G; g += 32) {
-      const uint4 a = __ldg(dr + g);
-      const float sa = half_to_f32(__ldg(dsr + g));
+      const float sa = half_to_f32(__ldg(dsr + g * f.sstep));
       float pa[NT];
-      group_dot<NT>(a, hs, row_len, g, pa);
+      group_dot_fmt<FMT, NT>(dr, hs, row_len, g, pa);
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[t] = fmaf(sa, pa[t], acc[t]);
     }
@@ -190,6 +242,7 @@ __device__ inline void stage_rows(float* xs, const float* src, size_t src_stride
   }
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(kWarps * 32)
 gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
   extern __shared__ float xs[];
@@ -208,22 +261,24 @@ gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
     __syncthreads();
     stage_rows(xs, ws.xf, sh.H, run.tok, run.n, sh.H);
     __syncthreads();
-    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * I * (sh.H / 2);
-    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * I * (sh.H / 32);
+    const RowFmt f = row_fmt(sh, sh.H);
+    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * I * f.qb;
+    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * I * f.ns;
     const uint8_t* gq = (shared ? w.sh_gate_q : w.gate_q) + eq;
     const uint16_t* gs = (shared ? w.sh_gate_s : w.gate_s) + es;
     const uint8_t* uq = (shared ? w.sh_up_q : w.up_q) + eq;
     const uint16_t* us = (shared ? w.sh_up_s : w.up_s) + es;
     switch (run.n) {
-      case 1: gate_up_rows<1>(gq, gs, uq, us, sh.H, I, r0, xs, run, ws); break;
-      case 2: gate_up_rows<2>(gq, gs, uq, us, sh.H, I, r0, xs, run, ws); break;
-      case 3: gate_up_rows<3>(gq, gs, uq, us, sh.H, I, r0, xs, run, ws); break;
-      default: gate_up_rows<4>(gq, gs, uq, us, sh.H, I, r0, xs, run, ws); break;
+      case 1: gate_up_rows<FMT, 1>(gq, gs, uq, us, sh.H, I, f, r0, xs, run, ws); break;
+      case 2: gate_up_rows<FMT, 2>(gq, gs, uq, us, sh.H, I, f, r0, xs, run, ws); break;
+      case 3: gate_up_rows<FMT, 3>(gq, gs, uq, us, sh.H, I, f, r0, xs, run, ws); break;
+      default: gate_up_rows<FMT, 4>(gq, gs, uq, us, sh.H, I, f, r0, xs, run, ws); break;
     }
   }
   }
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(kWarps * 32)
 down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
   extern __shared__ float hs[];
@@ -241,15 +296,16 @@ down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
     __syncthreads();
     stage_rows(hs, ws.hbuf, ws.hstride, run.row, run.n, I);
     __syncthreads();
-    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * sh.H * (I / 2);
-    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * sh.H * (I / 32);
+    const RowFmt f = row_fmt(sh, I);
+    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * sh.H * f.qb;
+    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * sh.H * f.ns;
     const uint8_t* dq = (shared ? w.sh_down_q : w.down_q) + eq;
     const uint16_t* ds = (shared ? w.sh_down_s : w.down_s) + es;
     switch (run.n) {
-      case 1: down_rows<1>(dq, ds, sh.H, I, r0, hs, run, ws); break;
-      case 2: down_rows<2>(dq, ds, sh.H, I, r0, hs, run, ws); break;
-      case 3: down_rows<3>(dq, ds, sh.H, I, r0, hs, run, ws); break;
-      default: down_rows<4>(dq, ds, sh.H, I, r0, hs, run, ws); break;
+      case 1: down_rows<FMT, 1>(dq, ds, sh.H, I, f, r0, hs, run, ws); break;
+      case 2: down_rows<FMT, 2>(dq, ds, sh.H, I, f, r0, hs, run, ws); break;
+      case 3: down_rows<FMT, 3>(dq, ds, sh.H, I, f, r0, hs, run, ws); break;
+      default: down_rows<FMT, 4>(dq, ds, sh.H, I, f, r0, hs, run, ws); break;
     }
   }
   }
@@ -310,11 +366,12 @@ cudaError_t launch_gate_up(const moe_weights_t& w, const Shape& sh, int T, const
                            cudaStream_t s) {
   const int Imax = sh.n_shared ? max(sh.I, sh.Is) : sh.I;
   const size_t smem = static_cast<size_t>(kNT) * (sh.H / 32) * kGS * sizeof(float);
-  cudaError_t e = set_smem(reinterpret_cast<const void*>(gate_up_kernel), smem);
+  auto kern = sh.wfmt == MOE_W_INT8 ? gate_up_kernel<MOE_W_INT8> : gate_up_kernel<MOE_W_INT4>;
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
   const dim3 grid((Imax + kRows - 1) / kRows, min(nt, 65535));
-  gate_up_kernel<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
+  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
   return cudaGetLastError();
 }
 
@@ -322,11 +379,12 @@ cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T, const Wo
                         cudaStream_t s) {
   const int Imax = sh.n_shared ? max(sh.I, sh.Is) : sh.I;
   const size_t smem = static_cast<size_t>(kNT) * (Imax / 32) * kGS * sizeof(float);
-  cudaError_t e = set_smem(reinterpret_cast<const void*>(down_kernel), smem);
+  auto kern = sh.wfmt == MOE_W_INT8 ? down_kernel<MOE_W_INT8> : down_kernel<MOE_W_INT4>;
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
   const dim3 grid((sh.H + kRows - 1) / kRows, min(nt, 65535));
-  down_kernel<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
+  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
   return cudaGetLastError();
 }
 

@@ -50,7 +50,19 @@ struct Workspace {
 struct Shape {
   int H, I, Is, E, k, n_group, topk_group, n_shared;
   float rsf;
+  int wfmt = 0;  // moe_wformat_t of the experts
+  int gsz = 32;  // scale group along K: 32, or 0 for one scale a row
 };
+
+// Bytes of one K-long weight row and its scales in the shape's format.
+__host__ __device__ inline size_t row_bytes(const Shape& sh, int K) {
+  return sh.wfmt == MOE_W_INT8 ? static_cast<size_t>(K) : static_cast<size_t>(K) / 2;
+}
+__host__ __device__ inline size_t row_scales(const Shape& sh, int K) {
+  return sh.gsz == 0 ? 1 : static_cast<size_t>(K) / 32;
+}
+// grouped int4: the format of the tensor-core paths
+__host__ __device__ inline bool grouped_int4(const Shape& sh) { return sh.wfmt == MOE_W_INT4 && sh.gsz == 32; }
 
 }  // namespace moe
 

@@ -571,6 +571,7 @@ int imax_of(const Shape& sh) { return sh.n_shared && sh.Is > sh.I ? sh.Is : sh.I
 }  // namespace tc
 
 bool tc_path_ok(const Shape& sh) {
+  if (!grouped_int4(sh)) return false;
   if (sh.H % 256 != 0 || sh.I % 256 != 0) return false;
   if (sh.n_shared && sh.Is % 256 != 0) return false;
   return true;

@@ -44,7 +44,10 @@ class moe_config_t(C.Structure):
                 ("top_k", C.c_int), ("n_group", C.c_int), ("topk_group", C.c_int),
                 ("routed_scaling_factor", C.c_float), ("n_shared", C.c_int),
                 ("shared_inter", C.c_int), ("group_size", C.c_int),
-                ("max_tokens", C.c_int)]
+                ("max_tokens", C.c_int), ("weight_format", C.c_int)]
+
+
+MOE_W_INT4, MOE_W_INT8 = 0, 1
 
 
 class moe_weights_t(C.Structure):
@@ -199,10 +202,11 @@ def moe_trace_read(h, cap: int):
 # ---------------------------------------------------------- torch wrapper --
 
 def config_for(shape, max_tokens: int) -> moe_config_t:
+    fmt = MOE_W_INT8 if getattr(shape, "weight_format", "int4") == "int8" else MOE_W_INT4
     return moe_config_t(shape.hidden, shape.inter, shape.n_experts, shape.top_k,
                         shape.n_group, shape.topk_group, shape.routed_scaling_factor,
                         shape.n_shared, shape.i_shared if shape.n_shared else 0,
-                        shape.group_size, max_tokens)
+                        shape.group_size, max_tokens, fmt)
 
 
 def weights_for(L) -> moe_weights_t:

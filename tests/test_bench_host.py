@@ -28,6 +28,15 @@ def test_expert_bytes_match_the_format(bench):
     for name, per_expert in (("glm_decode", 21_233_664), ("tiny", 55_296)):
         sh = CONFIGS[name].shape
         assert bench.expert_gate_up_bytes(sh) + bench.expert_down_bytes(sh) == per_expert
+    # one fp16 scale a row: 3 x 6144 x 2048 / 2 B of nibbles + (2 x 2048 +
+    # 6144) scales x 2 B = 18,874,368 + 20,480
+    sh = CONFIGS["glm_decode_rowscale"].shape
+    assert bench.expert_gate_up_bytes(sh) + bench.expert_down_bytes(sh) == 18_894_848
+    # int8, grouped: twice the weight bytes, the same scales
+    from workloads.configs import LayerShape
+    sh8 = LayerShape(6144, 2048, 256, 8, 8, 4, 2.5, weight_format="int8")
+    assert bench.expert_gate_up_bytes(sh8) + bench.expert_down_bytes(sh8) == \
+        2 * 18_874_368 + 21_233_664 - 18_874_368
 
 
 def test_single_token_bytes_are_the_per_token_figure(bench):

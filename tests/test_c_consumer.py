@@ -21,13 +21,16 @@ static int fails = 0;
 #define CHECK(c) do { if (!(c)) { printf("FAIL line %d: %s\n", __LINE__, #c); ++fails; } } while (0)
 
 int main(void) {
-  moe_config_t glm = {6144, 2048, 256, 8, 8, 4, 2.5f, 1, 2048, 32, 512};
-  moe_config_t bad = glm;
+  moe_config_t glm = {6144, 2048, 256, 8, 8, 4, 2.5f, 1, 2048, 32, 512, MOE_W_INT4};
+  moe_config_t bad = glm, row8 = glm;
   moe_layer_t* h = (moe_layer_t*)1;
   int32_t flags = 0;
   bad.group_size = 64;
+  row8.group_size = 0; /* one scale a row */
+  row8.weight_format = MOE_W_INT8;
   /* a valid config has a workspace, an invalid one has none */
   CHECK(moe_workspace_bytes(&glm) > 0);
+  CHECK(moe_workspace_bytes(&row8) == moe_workspace_bytes(&glm));
   CHECK(moe_workspace_bytes(&bad) == 0);
   CHECK(moe_workspace_bytes(NULL) == 0);
   /* argument errors come back before any CUDA call */

@@ -69,6 +69,7 @@ def test_workspace_bytes(m):
     dict(n_experts=2048), dict(n_group=3), dict(topk_group=5), dict(top_k=0),
     dict(top_k=33), dict(top_k=9, topk_group=2), dict(group_size=64), dict(max_tokens=0),
     dict(n_shared=2), dict(shared_inter=100), dict(routed_scaling_factor=float("nan")),
+    dict(group_size=16), dict(group_size=-1), dict(weight_format=2), dict(weight_format=-1),
 ])
 def test_bad_configs_are_unsupported(m, bad):
     h = C.c_void_p()
@@ -179,3 +180,13 @@ def test_route_noalloc_config_checks(m):
     assert "multiple of n_group" in m.moe_last_error(None)
     st = f(None, None, None, None, 0, 0, None, 0.0, None, None)
     assert st == -2 and "cfg is NULL" in m.moe_last_error(None)
+
+
+@pytest.mark.parametrize("fmt", [dict(group_size=0), dict(weight_format=1),
+                                 dict(weight_format=1, group_size=0)])
+def test_other_formats_are_accepted(m, fmt):
+    """int8 experts and one scale a row are valid configurations (the
+    workspace size does not depend on the format)."""
+    lib = m.load()
+    assert lib.moe_workspace_bytes(C.byref(_cfg(m, **fmt))) == \
+        lib.moe_workspace_bytes(C.byref(_cfg(m)))

@@ -8,6 +8,8 @@ glm_stack     24 such layers resident, T=1, RMSNorm before each router and a
               residual add after each layer
 glm_prefill_uniform  the same layer, T=8192 without the Zipf skew (256 rows
               per expert on average): the grouped GEMM where it is compute-bound
+glm_decode_rowscale  glm_decode with one fp16 scale per row (Colibri's whole-row
+              group, "GLM-5.2 on a 32 GB Mac", G2 implementation status)
 
 GLM-5.2 layer geometry (256 routed experts, top-8, one shared expert,
 routed_scaling_factor, sigmoid noaux_tc routing): "GLM-5.2 on a 32 GB Mac"
@@ -75,6 +77,7 @@ class Workload:
 
 TINY = LayerShape(256, 128, 16, 4, 4, 2, 2.5)
 GLM = LayerShape(6144, 2048, 256, 8, 8, 4, 2.5)
+GLM_ROWSCALE = LayerShape(6144, 2048, 256, 8, 8, 4, 2.5, group_size=0)
 
 CONFIGS = {
     "tiny": Workload("tiny", TINY, 1, 1, "f32", "uniform", 1001),
@@ -88,6 +91,8 @@ CONFIGS = {
     # without the Zipf skew, 256 plan rows per expert on average
     "glm_prefill_uniform": Workload("glm_prefill_uniform", GLM, 8192, 1, "bf16", "uniform",
                                     1005, extra={"bound": "tensor"}),
+    "glm_decode_rowscale": Workload("glm_decode_rowscale", GLM_ROWSCALE, 1, 256, "bf16", "zipf",
+                                    1006),
 }
 
 
