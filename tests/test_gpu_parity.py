@@ -598,3 +598,24 @@ def test_glm_stack_teacher_forced(m):
         assert err.max() <= TOL, (i, err)
     for h in handles:
         h.close()
+
+
+def test_two_handles_after_a_larger_shared_memory_shape(m):
+    """The single-token kernel's shared-memory opt-in is kept per kernel and
+    device: a handle whose shape needs more dynamic shared memory runs first,
+    then a handle of a smaller shape on the same device, then the first one
+    again; every call matches the oracle."""
+    big = LayerShape(6144, 1024, 64, 4, 4, 2, 2.5)    # ~197 KB: x_hat and rings of H = 6144
+    small = LayerShape(1024, 512, 32, 4, 4, 2, 2.5)
+    wb = Workload("smem_big", big, 1, 1, "bf16", "zipf", 9601)
+    ws_ = Workload("smem_small", small, 1, 1, "bf16", "zipf", 9602)
+    Lb, Ls = gen_layer(wb, device=DEV), gen_layer(ws_, device=DEV)
+    hb, hs = m.MoELayer(Lb, 1), m.MoELayer(Ls, 1)
+    for wl, L, h in ((wb, Lb, hb), (ws_, Ls, hs), (wb, Lb, hb), (ws_, Ls, hs)):
+        m.moe_trace_enable(h.h, 1)
+        _run_full(m, wl, L, gen_activations(wl, 1, call=0), handle=h)
+        names, rows = m.moe_trace_read(h.h, 1)
+        m.moe_trace_enable(h.h, 0)
+        assert {n for n, v in zip(names, rows[0]) if v > 0} == {"decode_fused"}
+    hb.close()
+    hs.close()
