@@ -17,8 +17,9 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU
 
 Without --workload the run measures glm_decode (the headline line) and then,
 at one GPU, glm_verify, glm_prefill, glm_stack, glm_prefill_uniform and
-glm_decode_rowscale (one scale a row) as sub-records of the same line, each
-timed for at least 1.5 s with its own clock record.
+glm_decode_rowscale and glm_prefill_rowscale (one scale a row) as
+sub-records of the same line, each timed for at least 1.5 s with its own
+clock record.
 """
 from __future__ import annotations
 
@@ -473,7 +474,7 @@ def run_reference(args, wl):
 # The workloads the default run measures after the headline (one process, one
 # after another, each layer stack freed before the next is generated).
 SUB_WORKLOADS = ("glm_verify", "glm_prefill", "glm_stack", "glm_prefill_uniform",
-                 "glm_decode_rowscale")
+                 "glm_decode_rowscale", "glm_prefill_rowscale")
 # A sub-record's timed region lasts at least this long, so that the 200 ms
 # clock sampler sees several samples under load.
 SUB_MIN_TIMED_S = 1.5
@@ -666,7 +667,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
-                             "glm_prefill_uniform", "glm_decode_rowscale"],
+                             "glm_prefill_uniform", "glm_decode_rowscale",
+                             "glm_prefill_rowscale"],
                     help="one workload only (default: glm_decode, then the other GLM "
                          "workloads as sub-records)")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")

@@ -90,10 +90,9 @@ typedef enum { MOE_W_INT4 = 0, MOE_W_INT8 = 1 } moe_wformat_t;
  *   top_k <= topk_group * (n_experts / n_group);
  *   group_size 32 or 0; weight_format MOE_W_INT4 or MOE_W_INT8;
  *   n_shared in {0, 1}; 1 <= max_tokens <= 65536.
- * The tensor-core paths (grouped GEMM, single-token tensor-core kernel) take
- * grouped int4 only; a handle of another format runs T = 1 on the
- * single-token SIMT kernel (per-row int4) or the SIMT batch path, and
- * T > 1 on the SIMT batch path. */
+ * int4 in either scale layout runs every path but the single-token
+ * tensor-core kernel (grouped int4 only); int8 runs on the SIMT batch path
+ * at every T. */
 typedef struct {
   int hidden;                  /* H */
   int inter;                   /* I, routed expert intermediate size */

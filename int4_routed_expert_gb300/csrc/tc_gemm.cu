@@ -18,7 +18,10 @@
 // Structure (one persistent CTA per SM, 23 warps):
 //   warp 20      TMA producer of the weights: per 256-wide K stage, the int4
 //                tile of 128 weight rows (128-byte swizzled) and its f16
-//                scales, into a 7-deep shared-memory ring.
+//                scales, into a 7-deep shared-memory ring.  With one scale
+//                a row ("G2 implementation status": Colibri's whole-row
+//                group) only the tile is copied: each dequantiser thread
+//                reads its row's scale once per item instead.
 //   warp 21      TMA producer of the activations: per stage up to 64 f16
 //                rows (four 64-wide K slabs, 128-byte swizzled), 3-deep ring.
 //   warps 0..15  dequantisers: each thread owns one weight row (TMEM lane)
@@ -60,6 +63,10 @@ struct TcMaps {
   CUtensorMap dn_s[2];     // scales, box 8 x 128
   CUtensorMap x16;         // [R][H] f16 activations, box 64 x 16
   CUtensorMap h16;         // [R][Imax] f16 SwiGLU rows, box 64 x 16
+  // one scale a row: [routed, shared][gate, up, down] scale arrays (the
+  // scale maps above are then unused)
+  const uint16_t* rs[2][3];
+  int row_scaled;
 };
 
 namespace tc {
@@ -98,6 +105,8 @@ struct Args {
   CUtensorMap aq[2][2];  // [routed, shared][gate, up] (down: [..][0])
   CUtensorMap as[2][2];
   CUtensorMap b;
+  const uint16_t* rs[2][2];  // one scale a row: [routed, shared][gate, up] (down: [..][0])
+  int row_scaled;
   Workspace ws;
   int T, N, H, I, Is, Imax;
   int mt_r, mt_s;    // M tiles per chunk (routed, shared)
@@ -281,15 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           fence_proxy_async_smem();
           const uint32_t full = smem_u32(wfull + s);
           const uint32_t base = smem_u32(wring + s * kWBytes);
-          mbar_arrive_expect_tx(full, kWBytes);
+          mbar_arrive_expect_tx(full, a.row_scaled ? kAQBytes : kWBytes);
           if (MODE == 0) {
             tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
             tma_load_2d_hint(base + 8192, &a.aq[sh][1], ks * 128, ya, full, pol);
-            tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
-            tma_load_2d_hint(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full, pol);
+            if (!a.row_scaled) {
+              tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
+              tma_load_2d_hint(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full, pol);
+            }
           } else {
             tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
-            tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
+            if (!a.row_scaled)
+              tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
           }
         }
         __syncwarp();
@@ -377,12 +389,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int q = warp & 3, j = warp >> 2;
     const int R = tile_row<MODE>(32 * q + lane);  // tile row of this thread's TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // one scale a row: this thread's row scale of an item (the item's weight
+    // rows start at the producer's ya; tile rows R & 63 of gate or up, or R)
+    auto row_scale = [&](const Item& t) -> uint32_t {
+      if (!a.row_scaled || t.n == 0) return 0u;
+      const int sh = t.e < 0 ? 1 : 0;
+      const size_t ya = MODE == 0 ? static_cast<size_t>(sh ? 0 : t.e) * a.I + 64 * t.mt
+                                  : static_cast<size_t>(sh ? 0 : t.e) * a.H + 128 * t.mt;
+      const uint16_t* p = MODE == 0 ? a.rs[sh][R < 64 ? 0 : 1] + ya + (R & 63) : a.rs[sh][0] + ya + R;
+      return __ldg(p);
+    };
     uint32_t it = 0;
     bool failed = false;
     Item tn = item_or_empty(a, blockIdx.x, total);
+    uint32_t srow_n = row_scale(tn);  // loaded one item ahead
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
       const Item t = tn;
       tn = item_or_empty(a, i + gridDim.x, total);
+      const uint32_t srow = srow_n;
+      srow_n = row_scale(tn);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int s = it % kWStages, ab = it % kABufs;
@@ -391,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         const unsigned char* st = wring + s * kWBytes;
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(st + kAQBytes + R * 16 + 4 * j);
+        const uint32_t sc = a.row_scaled
+                                ? (srow | (srow << 16))
+                                : *reinterpret_cast<const uint32_t*>(st + kAQBytes + R * 16 + 4 * j);
         const uint4 w0 = *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j) ^ (R & 7)) << 4));
         const uint4 w1 =
             *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j + 1) ^ (R & 7)) << 4));
@@ -571,7 +598,7 @@ int imax_of(const Shape& sh) { return sh.n_shared && sh.Is > sh.I ? sh.Is : sh.I
 }  // namespace tc
 
 bool tc_path_ok(const Shape& sh) {
-  if (!grouped_int4(sh)) return false;
+  if (sh.wfmt != MOE_W_INT4) return false;  // int4, grouped or one scale a row
   if (sh.H % 256 != 0 || sh.I % 256 != 0) return false;
   if (sh.n_shared && sh.Is % 256 != 0) return false;
   return true;
@@ -592,19 +619,27 @@ TcMaps* tc_create_maps(const moe_weights_t& w, const Shape& sh, const Workspace&
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, U16 = CU_TENSOR_MAP_DATA_TYPE_UINT16,
              F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   bool ok = true;
+  const bool gs = sh.gsz != 0;  // grouped scales: by TMA; one a row: read by the dequantisers
+  m->row_scaled = gs ? 0 : 1;
+  m->rs[0][0] = w.gate_s;
+  m->rs[0][1] = w.up_s;
+  m->rs[0][2] = w.down_s;
+  m->rs[1][0] = w.sh_gate_s;
+  m->rs[1][1] = w.sh_up_s;
+  m->rs[1][2] = w.sh_down_s;
   ok = ok && encode_2d(&m->gu_q[0][0], w.gate_q, U8, 1, H / 2, E * I, 128, 64, true);
   ok = ok && encode_2d(&m->gu_q[0][1], w.up_q, U8, 1, H / 2, E * I, 128, 64, true);
-  ok = ok && encode_2d(&m->gu_s[0][0], w.gate_s, U16, 2, H / 32, E * I, 8, 64, false);
-  ok = ok && encode_2d(&m->gu_s[0][1], w.up_s, U16, 2, H / 32, E * I, 8, 64, false);
+  ok = ok && (!gs || encode_2d(&m->gu_s[0][0], w.gate_s, U16, 2, H / 32, E * I, 8, 64, false));
+  ok = ok && (!gs || encode_2d(&m->gu_s[0][1], w.up_s, U16, 2, H / 32, E * I, 8, 64, false));
   ok = ok && encode_2d(&m->dn_q[0], w.down_q, U8, 1, I / 2, E * H, 128, 128, true);
-  ok = ok && encode_2d(&m->dn_s[0], w.down_s, U16, 2, I / 32, E * H, 8, 128, false);
+  ok = ok && (!gs || encode_2d(&m->dn_s[0], w.down_s, U16, 2, I / 32, E * H, 8, 128, false));
   if (sh.n_shared) {
     ok = ok && encode_2d(&m->gu_q[1][0], w.sh_gate_q, U8, 1, H / 2, Is, 128, 64, true);
     ok = ok && encode_2d(&m->gu_q[1][1], w.sh_up_q, U8, 1, H / 2, Is, 128, 64, true);
-    ok = ok && encode_2d(&m->gu_s[1][0], w.sh_gate_s, U16, 2, H / 32, Is, 8, 64, false);
-    ok = ok && encode_2d(&m->gu_s[1][1], w.sh_up_s, U16, 2, H / 32, Is, 8, 64, false);
+    ok = ok && (!gs || encode_2d(&m->gu_s[1][0], w.sh_gate_s, U16, 2, H / 32, Is, 8, 64, false));
+    ok = ok && (!gs || encode_2d(&m->gu_s[1][1], w.sh_up_s, U16, 2, H / 32, Is, 8, 64, false));
     ok = ok && encode_2d(&m->dn_q[1], w.sh_down_q, U8, 1, Is / 2, H, 128, 128, true);
-    ok = ok && encode_2d(&m->dn_s[1], w.sh_down_s, U16, 2, Is / 32, H, 8, 128, false);
+    ok = ok && (!gs || encode_2d(&m->dn_s[1], w.sh_down_s, U16, 2, Is / 32, H, 8, 128, false));
   }
   ok = ok && encode_2d(&m->x16, ws.x16, F16, 2, H, R, 64, 16, true);
   ok = ok && encode_2d(&m->h16, ws.h16, F16, 2, imax_of(sh), R, 64, 16, true);
@@ -659,6 +694,11 @@ cudaError_t launch_tc_gemm(const TcMaps& m, const Shape& sh, int T, const Worksp
   // the front end (T <= 4) builds chunks of at most 32 rows, within 64
   a.chunk = tc_chunk_rows(sh, T);
   a.n_sh_chunks = sh.n_shared ? (T + a.chunk - 1) / a.chunk : 0;
+  a.row_scaled = m.row_scaled;
+  for (int e = 0; e < 2; ++e) {
+    a.rs[e][0] = mode == 0 ? m.rs[e][0] : m.rs[e][2];
+    a.rs[e][1] = mode == 0 ? m.rs[e][1] : nullptr;
+  }
   if (mode == 0) {
     a.aq[0][0] = m.gu_q[0][0];
     a.aq[0][1] = m.gu_q[0][1];

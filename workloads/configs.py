@@ -10,6 +10,7 @@ glm_prefill_uniform  the same layer, T=8192 without the Zipf skew (256 rows
               per expert on average): the grouped GEMM where it is compute-bound
 glm_decode_rowscale  glm_decode with one fp16 scale per row (Colibri's whole-row
               group, "GLM-5.2 on a 32 GB Mac", G2 implementation status)
+glm_prefill_rowscale glm_prefill with one fp16 scale per row
 
 GLM-5.2 layer geometry (256 routed experts, top-8, one shared expert,
 routed_scaling_factor, sigmoid noaux_tc routing): "GLM-5.2 on a 32 GB Mac"
@@ -93,6 +94,8 @@ CONFIGS = {
                                     1005, extra={"bound": "tensor"}),
     "glm_decode_rowscale": Workload("glm_decode_rowscale", GLM_ROWSCALE, 1, 256, "bf16", "zipf",
                                     1006),
+    "glm_prefill_rowscale": Workload("glm_prefill_rowscale", GLM_ROWSCALE, 512, 1, "bf16", "zipf",
+                                     1007),
 }
 
 
