@@ -20,8 +20,9 @@
 //                tile of 128 weight rows (128-byte swizzled) and its f16
 //                scales, into a 7-deep shared-memory ring.  With one scale
 //                a row ("G2 implementation status": Colibri's whole-row
-//                group) only the tile is copied: each dequantiser thread
-//                reads its row's scale once per item instead.
+//                group) only the tile is copied: the dequantisers emit the
+//                exact u - 8 and the epilogue multiplies each row's f32
+//                accumulator by the row's scale (constant along K).
 //   warp 21      TMA producer of the activations: per stage up to 64 f16
 //                rows (four 64-wide K slabs, 128-byte swizzled), 3-deep ring.
 //   warps 0..15  dequantisers: each thread owns one weight row (TMEM lane)
@@ -182,6 +183,17 @@ __device__ __forceinline__ void dq_word_f16(uint32_t v, __half2 s2, uint32_t* ou
   out[3] = h2u(__hmul2(d, s2));
 }
 
+// The same without the scale: four f16 pairs u - 8, exact (one scale a row:
+// the row's scale multiplies the f32 accumulator in the epilogue instead).
+__device__ __forceinline__ void dq_word_f16_raw(uint32_t v, uint32_t* out) {
+  const __half2 k1032 = u2h(0x64086408u), k16 = u2h(0x2C002C00u), km72 = u2h(0xD480D480u);
+  const uint32_t v8 = v >> 8;
+  out[0] = h2u(__hsub2(u2h(lop(v, 0x000F000Fu)), k1032));
+  out[1] = h2u(__hfma2(u2h(lop(v, 0x00F000F0u)), k16, km72));
+  out[2] = h2u(__hsub2(u2h(lop(v8, 0x000F000Fu)), k1032));
+  out[3] = h2u(__hfma2(u2h(lop(v8, 0x00F000F0u)), k16, km72));
+}
+
 // One lane of a converged warp (the lowest active lane).
 __device__ __forceinline__ bool elect_one() {
   uint32_t p;
@@ -211,7 +223,8 @@ __device__ __forceinline__ int tile_row(int L) {
   return l < 16 ? 16 * q + l : 48 + 16 * q + l;
 }
 
-template <int MODE, int NMAX>  // MODE 0: gate/up, 1: down
+// MODE 0: gate/up, 1: down; RS: one scale a row (else grouped scales)
+template <int MODE, int NMAX, bool RS>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Args a) {
   using C = Cfg<NMAX>;
   constexpr int kWStages = C::kWStages, kBStages = C::kBStages, kABufs = C::kABufs;
@@ -290,17 +303,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           fence_proxy_async_smem();
           const uint32_t full = smem_u32(wfull + s);
           const uint32_t base = smem_u32(wring + s * kWBytes);
-          mbar_arrive_expect_tx(full, a.row_scaled ? kAQBytes : kWBytes);
+          mbar_arrive_expect_tx(full, RS ? kAQBytes : kWBytes);
           if (MODE == 0) {
             tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
             tma_load_2d_hint(base + 8192, &a.aq[sh][1], ks * 128, ya, full, pol);
-            if (!a.row_scaled) {
+            if (!RS) {
               tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
               tma_load_2d_hint(base + kAQBytes + 1024, &a.as[sh][1], ks * 8, ya, full, pol);
             }
           } else {
             tma_load_2d_hint(base, &a.aq[sh][0], ks * 128, ya, full, pol);
-            if (!a.row_scaled)
+            if (!RS)
               tma_load_2d_hint(base + kAQBytes, &a.as[sh][0], ks * 8, ya, full, pol);
           }
         }
@@ -389,25 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int q = warp & 3, j = warp >> 2;
     const int R = tile_row<MODE>(32 * q + lane);  // tile row of this thread's TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    // one scale a row: this thread's row scale of an item (the item's weight
-    // rows start at the producer's ya; tile rows R & 63 of gate or up, or R)
-    auto row_scale = [&](const Item& t) -> uint32_t {
-      if (!a.row_scaled || t.n == 0) return 0u;
-      const int sh = t.e < 0 ? 1 : 0;
-      const size_t ya = MODE == 0 ? static_cast<size_t>(sh ? 0 : t.e) * a.I + 64 * t.mt
-                                  : static_cast<size_t>(sh ? 0 : t.e) * a.H + 128 * t.mt;
-      const uint16_t* p = MODE == 0 ? a.rs[sh][R < 64 ? 0 : 1] + ya + (R & 63) : a.rs[sh][0] + ya + R;
-      return __ldg(p);
-    };
     uint32_t it = 0;
     bool failed = false;
     Item tn = item_or_empty(a, blockIdx.x, total);
-    uint32_t srow_n = row_scale(tn);  // loaded one item ahead
     for (int i = blockIdx.x; i < total && !failed; i += gridDim.x) {
       const Item t = tn;
       tn = item_or_empty(a, i + gridDim.x, total);
-      const uint32_t srow = srow_n;
-      srow_n = row_scale(tn);
       const int KS = t.e < 0 ? a.ks_s : a.ks_r;
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int s = it % kWStages, ab = it % kABufs;
@@ -416,9 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         const unsigned char* st = wring + s * kWBytes;
-        const uint32_t sc = a.row_scaled
-                                ? (srow | (srow << 16))
-                                : *reinterpret_cast<const uint32_t*>(st + kAQBytes + R * 16 + 4 * j);
+        const uint32_t sc =
+            RS ? 0u : *reinterpret_cast<const uint32_t*>(st + kAQBytes + R * 16 + 4 * j);
         const uint4 w0 = *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j) ^ (R & 7)) << 4));
         const uint4 w1 =
             *reinterpret_cast<const uint4*>(st + R * 128 + (((2 * j + 1) ^ (R & 7)) << 4));
@@ -429,17 +428,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         fence_after_sync();
-        const __half2 s0 = u2h((sc & 0xFFFFu) | (sc << 16));
-        const __half2 s1 = u2h((sc >> 16) | (sc & 0xFFFF0000u));
         uint32_t v[32];
-        dq_word_f16(w0.x, s0, v + 0);
-        dq_word_f16(w0.y, s0, v + 4);
-        dq_word_f16(w0.z, s0, v + 8);
-        dq_word_f16(w0.w, s0, v + 12);
-        dq_word_f16(w1.x, s1, v + 16);
-        dq_word_f16(w1.y, s1, v + 20);
-        dq_word_f16(w1.z, s1, v + 24);
-        dq_word_f16(w1.w, s1, v + 28);
+        if (RS) {
+          dq_word_f16_raw(w0.x, v + 0);
+          dq_word_f16_raw(w0.y, v + 4);
+          dq_word_f16_raw(w0.z, v + 8);
+          dq_word_f16_raw(w0.w, v + 12);
+          dq_word_f16_raw(w1.x, v + 16);
+          dq_word_f16_raw(w1.y, v + 20);
+          dq_word_f16_raw(w1.z, v + 24);
+          dq_word_f16_raw(w1.w, v + 28);
+        } else {
+          const __half2 s0 = u2h((sc & 0xFFFFu) | (sc << 16));
+          const __half2 s1 = u2h((sc >> 16) | (sc & 0xFFFF0000u));
+          dq_word_f16(w0.x, s0, v + 0);
+          dq_word_f16(w0.y, s0, v + 4);
+          dq_word_f16(w0.z, s0, v + 8);
+          dq_word_f16(w0.w, s0, v + 12);
+          dq_word_f16(w1.x, s1, v + 16);
+          dq_word_f16(w1.y, s1, v + 20);
+          dq_word_f16(w1.z, s1, v + 24);
+          dq_word_f16(w1.w, s1, v + 28);
+        }
         tmem_st32(tb + lane_base + 2 * NMAX + 128 * ab + 32 * j, v);
         tmem_wait_st();
         fence_before_sync();
@@ -451,11 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ---------------- epilogue (warps 16..19, TMEM lane quadrant warp % 4) ----------------
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // one scale a row: the scale of this thread's weight row (tile row R of
+    // TMEM lane 32q + lane) multiplies its accumulator, loaded one item ahead
+    const int R = tile_row<MODE>(32 * q + lane);
+    auto row_scale = [&](const Item& t) -> float {
+      if (!RS || t.n == 0) return 1.0f;
+      const int sh = t.e < 0 ? 1 : 0;
+      const size_t ya = MODE == 0 ? static_cast<size_t>(sh ? 0 : t.e) * a.I + 64 * t.mt
+                                  : static_cast<size_t>(sh ? 0 : t.e) * a.H + 128 * t.mt;
+      const uint16_t* p =
+          MODE == 0 ? a.rs[sh][R < 64 ? 0 : 1] + ya + (R & 63) : a.rs[sh][0] + ya + R;
+      return __half2float(__ushort_as_half(__ldg(p)));
+    };
     uint32_t ic = 0;
     Item tn = item_or_empty(a, blockIdx.x, total);
+    float srow_n = row_scale(tn);
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++ic) {
       const Item t = tn;
       tn = item_or_empty(a, i + gridDim.x, total);
+      const float srow = srow_n;
+      srow_n = row_scale(tn);
       const int d = ic & 1;
       if (!warp_wait(smem_u32(dfull + d), (ic >> 1) & 1, err)) break;
       fence_after_sync();
@@ -471,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             if (16 * c0 + c < t.n) {
-              const float g = __uint_as_float(v[c]);
+              const float g = RS ? __uint_as_float(v[c]) * srow : __uint_as_float(v[c]);
               const float u = __shfl_down_sync(0xffffffffu, g, 16);
               if (lane < 16) {
                 const float silu = g / (1.0f + expf(-g));
@@ -483,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           float* orow = a.ws.obuf + static_cast<size_t>(t.row0 + 16 * c0) * a.H + m;
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            if (16 * c0 + c < t.n) orow[static_cast<size_t>(c) * a.H] = __uint_as_float(v[c]);
+            if (16 * c0 + c < t.n)
+              orow[static_cast<size_t>(c) * a.H] = RS ? __uint_as_float(v[c]) * srow : __uint_as_float(v[c]);
         }
       }
       fence_before_sync();
@@ -666,15 +692,20 @@ cudaError_t launch_tc_prep(const Shape& sh, int T, const Workspace& ws, cudaStre
 
 namespace tc {
 namespace {
-template <int MODE, int NMAX>
-cudaError_t launch_gemm_inst(const Args& a, int n_sm, cudaStream_t s) {
+template <int MODE, int NMAX, bool RS>
+cudaError_t launch_gemm_rs(const Args& a, int n_sm, cudaStream_t s) {
   static std::atomic<size_t> attr_set[kMaxDevices];
   constexpr int smem = Cfg<NMAX>::kSmemBytes;
   const cudaError_t e =
-      opt_in_smem(reinterpret_cast<const void*>(tc_gemm_kernel<MODE, NMAX>), attr_set, smem);
+      opt_in_smem(reinterpret_cast<const void*>(tc_gemm_kernel<MODE, NMAX, RS>), attr_set, smem);
   if (e != cudaSuccess) return e;
-  tc_gemm_kernel<MODE, NMAX><<<n_sm, kThreads, smem, s>>>(a);
+  tc_gemm_kernel<MODE, NMAX, RS><<<n_sm, kThreads, smem, s>>>(a);
   return cudaGetLastError();
+}
+template <int MODE, int NMAX>
+cudaError_t launch_gemm_inst(const Args& a, int n_sm, cudaStream_t s) {
+  return a.row_scaled ? launch_gemm_rs<MODE, NMAX, true>(a, n_sm, s)
+                      : launch_gemm_rs<MODE, NMAX, false>(a, n_sm, s);
 }
 }  // namespace
 }  // namespace tc

@@ -84,8 +84,10 @@ def test_formats_match_the_oracle(m, fmt, gsz, shape):
 def test_row_scaled_equals_grouped_with_repeated_scales(m):
     """The pages' identity on the GPU: a per-row int4 layer and the same
     layer with each row's scale repeated over its groups give the same
-    outputs, on the single-token kernel (T = 1) and on the tensor-core
-    grouped GEMM (T = 3, 9): the same kernels, the same arithmetic."""
+    outputs bit for bit on the single-token kernel (T = 1: the same
+    arithmetic), and within the parity tolerance on the tensor-core grouped
+    GEMM (T = 3, 9), which rounds (u - 8) * s to f16 with grouped scales but
+    applies a row's scale to the f32 accumulator."""
     sh_r = LayerShape(1024, 512, 32, 4, 4, 2, 2.5, group_size=0)
     wl = Workload("rowscale", sh_r, 1, 1, "bf16", "zipf", 8201)
     Lr = gen_layer(wl, device=DEV)
@@ -102,7 +104,11 @@ def test_row_scaled_equals_grouped_with_repeated_scales(m):
         x = gen_activations(wl, T, call=c).to(DEV)
         yr, yg = hr.forward(x), hg.forward(x)
         torch.cuda.synchronize()
-        assert torch.equal(yr, yg), T
+        if T == 1:
+            assert torch.equal(yr, yg)
+        else:
+            d = (yr - yg).abs().amax(dim=1) / yg.abs().amax(dim=1)
+            assert float(d.max()) <= TOL, (T, d)
     hr.close()
     hg.close()
 
