@@ -180,7 +180,13 @@ moe_status_t moe_route(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
  * where E_e is routed expert e's SwiGLU and S the shared expert.  y: [T][H]
  * fp32.  y may alias x only for the residual-stream form (dtype MOE_F32,
  * accumulate = 1, rms_gamma != NULL, y == x exactly); otherwise they must
- * not overlap.  plan_out may be NULL.  T == 0 is a no-op. */
+ * not overlap.  plan_out may be NULL.  T == 0 is a no-op.
+ * x and y (and x of moe_route) are device memory, or pinned host memory that
+ * is mapped into the device's address space (cudaHostAlloc,
+ * cudaHostRegister): the kernels then read x and write y across the host
+ * link themselves, with no staging copy.  Any other pointer is refused with
+ * MOE_ERR_INVALID_ARG before a launch (each call asks the driver,
+ * cudaPointerGetAttributes). */
 moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
                          float* y, const float* rms_gamma, float rms_eps, int accumulate,
                          moe_plan_t* plan_out, void* stream);

@@ -486,6 +486,30 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
   return MOE_OK;
 }
 
+// x or y of a call as the kernels address it: device (or managed) memory as
+// it is, pinned host memory through its device mapping (the kernels then read
+// and write it across the host link, with no staging copy).  Other host
+// memory is refused before any launch.
+static moe_status_t resolve_io(moe_layer_t* h, const void* p, const void** out, const char* what) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    set_err(h, "%s: the CUDA driver does not know this pointer", what);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return MOE_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    *out = at.devicePointer;
+    return MOE_OK;
+  }
+  set_err(h, "%s must be device memory or pinned host memory mapped into the device's "
+             "address space", what);
+  return MOE_ERR_INVALID_ARG;
+}
+
 moe_status_t moe_route(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
                        const float* rms_gamma, float rms_eps, moe_plan_t* plan_out,
                        void* stream) {
@@ -495,6 +519,7 @@ moe_status_t moe_route(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
   }
   moe_status_t st = check_call(h, x, dtype, T, rms_gamma);
   if (st != MOE_OK || T == 0) return st;
+  if ((st = resolve_io(h, x, &x, "x")) != MOE_OK) return st;
   if ((st = check_plan(h, plan_out)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Tracer none;
@@ -531,6 +556,12 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
                  "rms_gamma, y == x) is allowed");
       return MOE_ERR_INVALID_ARG;
     }
+  }
+  if ((st = resolve_io(h, x, &x, "x")) != MOE_OK) return st;
+  {
+    const void* yd = nullptr;
+    if ((st = resolve_io(h, y, &yd, "y")) != MOE_OK) return st;
+    y = static_cast<float*>(const_cast<void*>(yd));
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Tracer tr;

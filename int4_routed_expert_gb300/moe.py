@@ -255,6 +255,7 @@ class MoELayer:
     def __init__(self, layer_inputs, max_tokens: int):
         self.inputs = layer_inputs  # keeps the weights alive
         self.shape = layer_inputs.shape
+        self.device = layer_inputs.router_w.device
         self.max_tokens = max_tokens
         self.cfg = config_for(self.shape, max_tokens)
         self.h = moe_layer_create(self.cfg, weights_for(layer_inputs))
@@ -279,18 +280,27 @@ class MoELayer:
             return MOE_BF16
         raise TypeError(f"x must be fp32 or bf16, got {x.dtype}")
 
+    @staticmethod
+    def _io_ok(t) -> bool:
+        """x and y may live on a CUDA device or in pinned host memory (the
+        kernels then read and write it across the host link)."""
+        return t.is_cuda or (t.device.type == "cpu" and t.is_pinned())
+
     def _check_x(self, x):
-        """x: a contiguous [T][hidden] fp32/bf16 tensor on a CUDA device; returns T."""
-        if not x.is_cuda or x.dim() != 2 or x.shape[1] != self.shape.hidden \
+        """x: a contiguous [T][hidden] fp32/bf16 tensor on a CUDA device or in
+        pinned host memory; returns T."""
+        if not self._io_ok(x) or x.dim() != 2 or x.shape[1] != self.shape.hidden \
                 or not x.is_contiguous():
-            raise ValueError(f"x must be a contiguous CUDA tensor of shape [T, "
-                             f"{self.shape.hidden}], got {tuple(x.shape)} on {x.device}")
+            raise ValueError(f"x must be a contiguous CUDA or pinned host tensor of shape "
+                             f"[T, {self.shape.hidden}], got {tuple(x.shape)} on {x.device}")
         return x.shape[0]
 
-    def _check_vec(self, t, name: str, rows: int, device):
-        """t: a contiguous fp32 tensor on ``device`` with rows * hidden elements."""
+    def _check_vec(self, t, name: str, rows: int, device, host_ok: bool = False):
+        """t: a contiguous fp32 tensor on ``device`` (or pinned host memory when
+        host_ok) with rows * hidden elements."""
         import torch
-        if t.device != device or t.dtype != torch.float32 or not t.is_contiguous() \
+        where_ok = t.device == device or (host_ok and self._io_ok(t))
+        if not where_ok or t.dtype != torch.float32 or not t.is_contiguous() \
                 or t.numel() != rows * self.shape.hidden:
             raise ValueError(f"{name} must be a contiguous fp32 tensor on {device} with "
                              f"{rows} x {self.shape.hidden} elements")
@@ -305,9 +315,9 @@ class MoELayer:
               stream=None) -> Plan:
         T = self._check_x(x)
         if gamma is not None:
-            self._check_vec(gamma, "gamma", 1, x.device)
-        plan = plan or Plan(T, self.shape.top_k, self.shape.n_experts, x.device)
-        plan.check(T, self.shape.top_k, self.shape.n_experts, x.device)
+            self._check_vec(gamma, "gamma", 1, self.device)
+        plan = plan or Plan(T, self.shape.top_k, self.shape.n_experts, self.device)
+        plan.check(T, self.shape.top_k, self.shape.n_experts, self.device)
         pc = plan.c()
         moe_route(self.h, x.data_ptr(), self._dtype(x), T,
                   gamma.data_ptr() if gamma is not None else None, eps, pc,
@@ -319,12 +329,12 @@ class MoELayer:
         import torch
         T = self._check_x(x)
         if y is None:
-            y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=x.device)
-        self._check_vec(y, "y", T, x.device)
+            y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=self.device)
+        self._check_vec(y, "y", T, self.device, host_ok=True)
         if gamma is not None:
-            self._check_vec(gamma, "gamma", 1, x.device)
+            self._check_vec(gamma, "gamma", 1, self.device)
         if plan is not None:
-            plan.check(T, self.shape.top_k, self.shape.n_experts, x.device)
+            plan.check(T, self.shape.top_k, self.shape.n_experts, self.device)
         pc = plan.c() if plan is not None else None
         moe_forward(self.h, x.data_ptr(), self._dtype(x), T, y.data_ptr(),
                     gamma.data_ptr() if gamma is not None else None, eps,

@@ -619,3 +619,37 @@ def test_two_handles_after_a_larger_shared_memory_shape(m):
         assert {n for n, v in zip(names, rows[0]) if v > 0} == {"decode_fused"}
     hb.close()
     hs.close()
+
+
+def test_pinned_host_inputs_and_outputs(m):
+    """x and y in pinned host memory (read and written by the kernels across
+    the host link) give the same outputs bit for bit as device buffers, on
+    the single-token kernel (T = 1), the routing front end (T = 3), the
+    routing kernels with the grouped GEMM (T = 9) and the SIMT batch path
+    (an int8 layer); unpinned host memory is refused before any launch."""
+    import ctypes as C
+    cases = [(LayerShape(1024, 512, 64, 6, 8, 3, 2.5), (1, 3, 9)),
+             (LayerShape(512, 256, 32, 4, 4, 2, 2.5, weight_format="int8"), (1, 9))]
+    for sh, Ts in cases:
+        wl = Workload("pinned_io", sh, 9, 1, "bf16", "zipf", 9801)
+        L = gen_layer(wl, device=DEV)
+        h = m.MoELayer(L, 16)
+        for T in Ts:
+            x = gen_activations(wl, T, call=T)
+            y_dev = h.forward(x.to(DEV))
+            xh = x.pin_memory()
+            yh = torch.empty(T, sh.hidden, dtype=torch.float32).pin_memory()
+            h.forward(xh, y=yh)
+            torch.cuda.synchronize()
+            assert torch.equal(yh, y_dev.cpu()), (sh, T)
+        assert m.moe_device_status(h.h) == 0
+        # the binding refuses unpinned host tensors ...
+        with pytest.raises(ValueError):
+            h.forward(gen_activations(wl, 1, call=0))
+        # ... and the C ABI refuses unregistered host memory before a launch
+        buf = np.zeros((1, sh.hidden), np.float32)
+        yd = torch.empty(1, sh.hidden, dtype=torch.float32, device=DEV)
+        st = m.load().moe_forward(h.h, C.c_void_p(buf.ctypes.data), m.MOE_F32, 1,
+                                  C.c_void_p(yd.data_ptr()), None, C.c_float(0.0), 0, None, None)
+        assert st == -1 and "pinned host memory" in m.moe_last_error(h.h)
+        h.close()
