@@ -25,7 +25,9 @@ bool decode_path_ok(const Shape& sh, int T, int n_sm) {
   const int epl = fast_select_epl(sh);
   if (epl < 1 || epl > 8) return false;
   if (n_sm < 1 || (sh.E + n_sm - 1) / n_sm > kMaxLocalExperts) return false;
-  if (sh.I % 256 != 0) return false;
+  // a down item's 4 rows of scales (I / 4 bytes) are one bulk copy: a
+  // multiple of 16 bytes
+  if (sh.I % 64 != 0) return false;
   if (sh.n_shared && sh.Is != sh.I) return false;
   if (!chunks_per_lane(sh.H)) return false;
   const int ci = chunks_per_lane(sh.I);

@@ -92,9 +92,9 @@ def test_tiny_layer(m, T):
 # ------------------------------------------------------------- shape sweep ---
 
 SHAPES = [
-    # H, I, E, k, n_group, topk_group, n_shared  (I % 256 == 0 and E <= 256 with
-    # E = 32 * 2^j take the fused single-token kernel for T = 1; T > 1 with
-    # I % 256 == 0 takes the grouped GEMM)
+    # H, I, E, k, n_group, topk_group, n_shared  (I % 64 == 0, I <= 2048 takes
+    # the fused single-token kernel for T = 1; T > 1 with I % 256 == 0 takes
+    # the grouped GEMM)
     (256, 256, 32, 4, 4, 2, 1),
     (512, 512, 64, 6, 8, 3, 1),
     (1024, 256, 128, 8, 8, 4, 1),
