@@ -580,8 +580,9 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
     if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (single-token tensor-core path)");
   } else if (fused) {
     moe::PhaseMarker pm{tr.on() ? &Tracer::mark_cb : nullptr, &tr};
+    // the plan reaches the workspace only when the caller asked for it
     e = moe::launch_decode(h->w, sh, T, x, dtype, rms_gamma, rms_eps, ws, y, accumulate,
-                           h->n_sm, &h->decode_calls, pm, s);
+                           plan_out != nullptr ? 1 : 0, h->n_sm, &h->decode_calls, pm, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "moe_forward (single-token path)");
   } else if (h->tc) {
     if (moe::front_path_ok(sh, T, h->n_sm)) {

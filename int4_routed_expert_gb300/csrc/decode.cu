@@ -37,8 +37,8 @@ bool decode_path_ok(const Shape& sh, int T, int n_sm) {
 
 cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const void* x,
                           moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,
-                          float* y, int accumulate, int n_sm, unsigned long long* calls,
-                          const PhaseMarker& pm, cudaStream_t s) {
+                          float* y, int accumulate, int write_plan, int n_sm,
+                          unsigned long long* calls, const PhaseMarker& pm, cudaStream_t s) {
   using namespace dec;
   DecArgs a;
   a.w = w;
@@ -51,6 +51,7 @@ cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const 
   a.ws = ws;
   a.y = y;
   a.accumulate = accumulate;
+  a.write_plan = write_plan;
   // every CTA adds one to the grid-barrier counter per barrier round;
   // *calls counts the rounds of this handle so far
   a.gtarget = (*calls + 1) * static_cast<unsigned long long>(n_sm);

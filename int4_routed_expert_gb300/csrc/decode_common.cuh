@@ -32,6 +32,7 @@ struct DecArgs {
   Workspace ws;
   float* y;
   int accumulate;
+  int write_plan = 1;  // the single-token kernels write the call's plan to the workspace
   unsigned long long gtarget;   // grid-barrier count that completes this call's first barrier
   unsigned long long gtarget2;  // ... and its second (fused single-token kernel)
 };

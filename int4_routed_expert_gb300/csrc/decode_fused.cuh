@@ -376,8 +376,10 @@ dec_fused_kernel(const __grid_constant__ DecArgs a) {
       if (lane == 0) s_nact = k;
       __syncwarp();
       if (lane == 0) mbar_arrive(planbar);
-      if (b == 0) {
-        // the plan of the call for moe_forward's plan output
+      if (b == 0 && a.write_plan) {
+        // the plan of the call for moe_forward's plan output (under load
+        // these stores hold warp 0 for several microseconds, so they are
+        // made only when the caller asked for the plan)
         if (lane < k) {
           ws.ids[lane] = id;
           ws.topw[lane] = w;

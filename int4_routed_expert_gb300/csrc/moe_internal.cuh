@@ -189,9 +189,10 @@ cudaError_t launch_dm(const dm::Maps& maps, const moe_weights_t& w, const Shape&
                       int accumulate, int n_sm, unsigned long long* calls, const PhaseMarker& pm,
                       cudaStream_t s);
 // calls: the handle's count of grid-barrier rounds (read and advanced).
+// write_plan: 0 leaves the workspace's plan arrays unwritten (no plan output).
 cudaError_t launch_decode(const moe_weights_t& w, const Shape& sh, int T, const void* x,
                           moe_dtype_t dt, const float* gamma, float eps, const Workspace& ws,
-                          float* y, int accumulate, int n_sm, unsigned long long* calls,
-                          const PhaseMarker& pm, cudaStream_t s);
+                          float* y, int accumulate, int write_plan, int n_sm,
+                          unsigned long long* calls, const PhaseMarker& pm, cudaStream_t s);
 
 }  // namespace moe
