@@ -679,6 +679,119 @@ def measure(args, wl, dev, world, steps, warmup, clocks, min_timed_s=0.0, layers
     return rec
 
 
+# The expert tier's record: glm_decode with the routed experts in pinned host
+# memory and a quarter of them in HBM slots, some pinned.
+TIER_SLOTS, TIER_PINNED = 64, 16
+
+
+def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S):
+    """glm_decode through the expert tier (moe_tier_forward).
+
+    The first warm-up step fills the slots and the use counts; the hot store
+    is then seeded with the most-used experts (repin into free capacity, "GLM-
+    5.2 on a 32 GB Mac", "What Colibri is actually doing", items 5-6).  A step
+    is timed by the wall clock: each call routes, reads its union to the host,
+    takes the slot decisions and copies its misses, so host time is part of
+    it; the step ends with a device synchronisation."""
+    import math
+
+    import torch
+
+    import int4_routed_expert_gb300 as m
+    from workloads.gen import gen_activations, gen_layer
+
+    wl = make_workload("glm_decode")
+    sh = wl.shape
+    L = gen_layer(wl, device=dev)
+    x = torch.stack([gen_activations(wl, 1, call=c) for c in range(wl.calls)]).to(dev)
+    y = torch.empty(wl.calls, 1, sh.hidden, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    tier = None
+
+    def step():
+        t0 = time.perf_counter()
+        for c in range(wl.calls):
+            tier.forward(x[c], y=y[c], stream=stream)
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    # the same path with a slot for every expert: after one step every call
+    # hits, so this is the cost of routing, read-back and the expert kernels
+    tier = m.ExpertTier(L, max_tokens=1, n_slots=sh.n_experts)
+    step()
+    resident_s = min(step() for _ in range(2))
+    tier.close()
+    tier = m.ExpertTier(L, max_tokens=1, n_slots=TIER_SLOTS, n_pinned=TIER_PINNED,
+                        drop_device_routed=True)
+    del L
+    torch.cuda.empty_cache()
+    # the host link: one routed array (all experts' gate weights) copied from
+    # its page-locked host copy into HBM
+    src = tier.host["gate_q"]
+    dst = torch.empty(src.shape, dtype=src.dtype, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    link_gbs = 0.0
+    for _ in range(3):
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        link_gbs = max(link_gbs, src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1e3)
+                       / 1e9)
+    del dst
+    torch.cuda.empty_cache()
+    step()
+    pins = tier.repin(0)
+    step_s = min(step() for _ in range(max(warmup, 3) - 1))
+    steps = max(1, int(math.ceil(min_timed_s / max(step_s, 1e-6))))
+    s0 = tier.query()[0]
+    clocks.wait_first()
+    t_start = clocks.now()
+    secs = sum(step() for _ in range(steps))
+    t_stop = clocks.now()
+    s1 = tier.query()[0]
+    d = {k: s1[k] - s0[k] for k in ("hits_pinned", "hits_lru", "misses", "loads", "evictions",
+                                    "h2d_bytes")}
+    tokens = steps * wl.calls
+    admitted = d["hits_pinned"] + d["hits_lru"] + d["misses"]
+    eb = sh.expert_bytes()
+    rec = {
+        "value": tokens / secs, "unit": UNIT, "steps": steps, "warmup": max(warmup, 3),
+        "ms_per_step": 1000.0 * secs / steps, "timed_s": round(secs, 3),
+        "config": {
+            "workload": "glm_decode_tier", "hidden": sh.hidden, "inter": sh.inter,
+            "n_experts": sh.n_experts, "top_k": sh.top_k, "tokens_per_call": 1,
+            "calls_per_step": wl.calls, "tokens_per_step": wl.calls,
+            "hbm_slots": TIER_SLOTS, "pinned_slots": TIER_PINNED,
+            "host_store_bytes": sh.n_experts * eb, "hbm_slot_bytes": TIER_SLOTS * eb,
+            "weights": "int4 offset-binary, group 32, fp16 scales",
+            "timing": "wall clock per step (routing, union read-back, slot decisions and "
+                      "host-to-HBM expert copies inside), device synchronised at the end "
+                      "of each step; L2 not flushed",
+        },
+        "tier": {
+            "hit_rate": round((d["hits_pinned"] + d["hits_lru"]) / max(admitted, 1), 4),
+            "pinned_hit_rate": round(d["hits_pinned"] / max(admitted, 1), 4),
+            "experts_per_token": round(admitted / tokens, 3),
+            "misses_per_token": round(d["misses"] / tokens, 3),
+            "evictions_per_token": round(d["evictions"] / tokens, 3),
+            "h2d_bytes_per_token": round(d["h2d_bytes"] / tokens, 1),
+            "h2d_gbs": round(d["h2d_bytes"] / secs / 1e9, 1),
+            "pins_seeded": pins,
+            "host_link_h2d_gbs": round(link_gbs, 1),
+            "copy_bound_tokens_per_s": round(link_gbs * 1e9 / max(d["h2d_bytes"] / tokens, 1), 1),
+            "all_resident_tokens_per_s": round(wl.calls / resident_s, 1),
+            "host_link_source": "cudaMemcpyAsync of one routed array (all experts' gate "
+                                "weights) from page-locked host memory into HBM, CUDA events",
+        },
+        "clocks": clocks.summary(t_start, t_stop),
+    }
+    tier.close()
+    del tier, x, y
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -688,7 +801,7 @@ def main():
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "glm_decode", "glm_verify", "glm_prefill", "glm_stack",
                              "glm_prefill_uniform", "glm_decode_rowscale",
-                             "glm_prefill_rowscale"],
+                             "glm_prefill_rowscale", "glm_decode_tier"],
                     help="one workload only (default: glm_decode, then the other GLM "
                          "workloads as sub-records)")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling only)")
@@ -701,6 +814,9 @@ def main():
     args = ap.parse_args()
     single = args.workload is not None
     name = args.workload or "glm_decode"
+    if name == "glm_decode_tier":
+        run_tier_only(args)
+        return
     wl = make_workload(name, args.experts, args.calls, args.tokens)
 
     if args.impl == "reference":
@@ -742,6 +858,7 @@ def main():
             swl = make_workload(sub)
             subs[sub] = measure(args, swl, dev, world, 1, args.warmup, clocks,
                                 min_timed_s=SUB_MIN_TIMED_S)
+        subs["glm_decode_tier"] = measure_tier(dev, clocks, args.warmup)
     clocks.stop()
 
     if rank == 0:
@@ -769,6 +886,24 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_tier_only(args):
+    """--workload glm_decode_tier: the tier's record alone, as one line."""
+    import torch
+    dev = "cuda:0"
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    clocks = ClockSampler(0)
+    clocks.start()
+    rec = measure_tier(dev, clocks, args.warmup)
+    clocks.stop()
+    line = {"metric": METRIC, "n_gpus": 1, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded int4 weights, fp16 scales, Zipf router bias)"}
+    line.update(rec)
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -296,6 +296,133 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* router_w,
                                int T, const float* rms_gamma, float rms_eps,
                                moe_plan_t* plan_out, void* stream);
 
+/* ---- Expert slot cache (host only) ---------------------------------------
+ *
+ * The residency policy of the expert tier below, as a plain host object so
+ * that its decisions can be driven and checked without a GPU.  "GLM-5.2 on a
+ * 32 GB Mac - native MLX port of the Colibri hierarchy", "What Colibri is
+ * actually doing": item 4 (per-layer bounded LRU with a monotonic use
+ * clock), item 5 (pinned hot store, never evicted), item 6 (live repinning
+ * with a 25 % + 4 hysteresis), item 8 (a call admits the union of its
+ * experts, each once).
+ *
+ * n_slots slots hold experts 0..n_experts-1; at most n_pinned of them are
+ * pinned; a call's union must fit in the unpinned ones, so
+ * n_slots - n_pinned >= call_slots.  Kinds written per expert: 0 = hit in
+ * the hot store, 1 = hit in an LRU slot, 2 = loaded (the slot must be
+ * filled; a resident expert may have been evicted for it).
+ *   admit     one call's distinct experts: hits advance the use clock in the
+ *             order given; a load takes the lowest free slot, else the least
+ *             recently used unpinned slot holding no expert of the set; every
+ *             expert counts one use
+ *   prefetch  the same placement, counting no use and leaving resident
+ *             experts as they are
+ *   pin       makes the experts resident and pins their slots
+ *   repin     at a safe point: pins the hottest resident unpinned experts
+ *             into free hot-store capacity, then up to max_swaps times
+ *             replaces the coldest pin (fewest uses, then the higher id) by
+ *             the hottest resident unpinned expert (most uses, then the lower
+ *             id) when uses(hot) > 1.25 uses(cold) + 4; returns the changes
+ *             (-1 for a NULL cache or max_swaps < 0)
+ *   query     counters; slot_of[e] = slot, -(slot + 2) when pinned, -1 when
+ *             absent; uses[e] = admissions of e (NULL outputs are skipped)
+ * An operation that fails (ids outside [0, n_experts) or repeated, more
+ * loads than free or evictable slots, too many pins) changes nothing and
+ * returns MOE_ERR_INVALID_ARG with the reason in moe_last_error(NULL).  A
+ * cache is used by one thread at a time. */
+typedef struct moe_slot_cache moe_slot_cache_t;
+typedef struct {
+  uint64_t hits_pinned; /* admitted experts found pinned */
+  uint64_t hits_lru;    /* admitted experts found in an LRU slot */
+  uint64_t misses;      /* admitted experts that were loaded */
+  uint64_t loads;       /* slots filled by admit, prefetch and pin */
+  uint64_t evictions;   /* resident experts displaced by a load */
+  int32_t n_resident;
+  int32_t n_pinned;
+} moe_slot_cache_stats_t;
+
+moe_status_t moe_slot_cache_create(int n_experts, int n_slots, int n_pinned, int call_slots,
+                                   moe_slot_cache_t** out);
+moe_status_t moe_slot_cache_admit(moe_slot_cache_t* c, const int32_t* ids, int n,
+                                  int32_t* slot, int32_t* kind);
+moe_status_t moe_slot_cache_prefetch(moe_slot_cache_t* c, const int32_t* ids, int n,
+                                     int32_t* slot, int32_t* kind);
+moe_status_t moe_slot_cache_pin(moe_slot_cache_t* c, const int32_t* ids, int n, int32_t* slot,
+                                int32_t* kind);
+int moe_slot_cache_repin(moe_slot_cache_t* c, int max_swaps);
+moe_status_t moe_slot_cache_query(const moe_slot_cache_t* c, moe_slot_cache_stats_t* stats,
+                                  int32_t* slot_of, uint64_t* uses);
+void moe_slot_cache_destroy(moe_slot_cache_t* c);
+
+/* ---- Expert tier: routed experts in host memory, a bounded set in HBM ----
+ *
+ * The GPU edition of the pages' expert hierarchy ("GLM-5.2 on a 32 GB Mac",
+ * "What Colibri is actually doing", items 4-10): the routed experts of a
+ * layer live in pinned host memory (reached over the host link) and
+ * tcfg->n_slots of them are held in HBM slots managed by the slot cache
+ * above; the router and the shared expert stay resident.
+ *
+ * moe_tier_create(cfg, w, tcfg, out): cfg as for moe_layer_create.  In w,
+ *   router_w, router_bias and sh_* are device pointers (as for
+ *   moe_layer_create); gate_q ... down_s are the routed arrays of all
+ *   n_experts in host memory that is page-locked (cudaHostAlloc or
+ *   cudaHostRegister), in the same layout; they are borrowed for the tier's
+ *   lifetime and only read.  The tier allocates the workspace, the HBM slots
+ *   (n_slots experts) and one copy stream.  Needs 1 <= n_slots <= n_experts,
+ *   0 <= n_pinned and n_slots - n_pinned >= min(n_experts,
+ *   max_tokens * top_k), so that one call's union always fits
+ *   (MOE_ERR_INVALID_ARG otherwise).
+ *
+ * moe_tier_forward: the layer of moe_forward (same arguments and result, y
+ *   within the same tolerance of the oracle), computed as follows:
+ *   1. route the tokens on `stream` and wait for the union of their experts
+ *      (a small device-to-host copy; the host blocks until routing is done);
+ *   2. admit the union in the slot cache; copy every loaded expert from host
+ *      memory into its slot on the copy stream (item 9: bounded async reads);
+ *   3. launch the experts that are resident (and the shared expert) first,
+ *      then, once the copies have landed, the loaded ones (item 9: resident
+ *      experts are submitted before the miss reads finish); then the
+ *      weighted combine.
+ *   The experts run on the SIMT batch kernels (every weight format).  A slot
+ *   is never read before its copy has completed and never overwritten while a
+ *   call that reads it may still run (item 10: no partially filled slot is
+ *   published).  All calls of one tier use one stream.
+ * moe_tier_prefetch(t, ids, n): loads the experts not yet resident (no use
+ *   counted) on the copy stream and returns without waiting (item 10).
+ * moe_tier_prefetch_routed(t, x, dtype, T, rms_gamma, rms_eps, stream):
+ *   routes x with this tier's router and prefetches the union (item 10,
+ *   PILOT: the next layer's router applied to the current state).  Waits
+ *   for the routing, not for the copies.
+ * moe_tier_pin(t, ids, n): loads (if needed) and pins experts (item 5).
+ * moe_tier_repin(t, max_swaps, changed): moe_slot_cache_repin at a safe
+ *   point; *changed (may be NULL) receives its result.
+ * moe_tier_query(t, stats, slot_of, uses, h2d_bytes): the slot cache's
+ *   query; *h2d_bytes (may be NULL) = expert bytes copied into HBM so far.
+ * moe_tier_last_error(t): the tier's last message (moe_last_error(NULL) for
+ *   failures of moe_tier_create).
+ * moe_tier_destroy(t): waits for the tier's work and frees it (NULL is
+ *   ignored). */
+typedef struct moe_tier moe_tier_t;
+typedef struct {
+  int n_slots;  /* HBM expert slots */
+  int n_pinned; /* of which the hot store may hold this many */
+} moe_tier_config_t;
+
+moe_status_t moe_tier_create(const moe_config_t* cfg, const moe_weights_t* w,
+                             const moe_tier_config_t* tcfg, moe_tier_t** out);
+moe_status_t moe_tier_forward(moe_tier_t* t, const void* x, moe_dtype_t dtype, int T, float* y,
+                              const float* rms_gamma, float rms_eps, int accumulate,
+                              moe_plan_t* plan_out, void* stream);
+moe_status_t moe_tier_prefetch(moe_tier_t* t, const int32_t* ids, int n);
+moe_status_t moe_tier_prefetch_routed(moe_tier_t* t, const void* x, moe_dtype_t dtype, int T,
+                                      const float* rms_gamma, float rms_eps, void* stream);
+moe_status_t moe_tier_pin(moe_tier_t* t, const int32_t* ids, int n);
+moe_status_t moe_tier_repin(moe_tier_t* t, int max_swaps, int* changed);
+moe_status_t moe_tier_query(moe_tier_t* t, moe_slot_cache_stats_t* stats, int32_t* slot_of,
+                            uint64_t* uses, uint64_t* h2d_bytes);
+const char* moe_tier_last_error(const moe_tier_t* t);
+void moe_tier_destroy(moe_tier_t* t);
+
 #ifdef __cplusplus
 }
 #endif

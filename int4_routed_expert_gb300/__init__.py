@@ -6,6 +6,8 @@ package holds its CUDA sources (``csrc/``), the in-tree build
 """
 from .moe import (  # noqa: F401
     EXPORTED,
+    ExpertTier,
+    SlotCache,
     MOE_BF16,
     MOE_F32,
     MoeError,

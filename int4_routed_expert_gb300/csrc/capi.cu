@@ -10,6 +10,7 @@
 #include <new>
 
 #include "moe_internal.cuh"
+#include "tier_internal.cuh"
 
 using moe::Shape;
 using moe::Workspace;
@@ -127,9 +128,11 @@ const char* check_extent(const void* p, size_t bytes, int device) {
   return nullptr;
 }
 
-const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, int device,
-                                const char** which) {
-  const size_t E = c->n_experts, H = c->hidden, I = c->inter;
+// E_routed: experts the routed arrays hold (n_experts, or the expert tier's
+// slots); the router arrays always hold n_experts.
+const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, size_t E_routed,
+                                int device, const char** which) {
+  const size_t E = c->n_experts, H = c->hidden, I = c->inter, Er = E_routed;
   // bytes of a K-long row's weights and of its scales, in the format
   auto qb = [&](size_t K) { return c->weight_format == MOE_W_INT8 ? K : K / 2; };
   auto sb = [&](size_t K) { return (c->group_size == 0 ? 1 : K / 32) * 2; };
@@ -140,12 +143,12 @@ const char* check_weight_memory(const moe_config_t* c, const moe_weights_t* w, i
   };
   const A routed[] = {{"router_w", w->router_w, E * H * 4},
                       {"router_bias", w->router_bias, E * 4},
-                      {"gate_q", w->gate_q, E * I * qb(H)},
-                      {"gate_s", w->gate_s, E * I * sb(H)},
-                      {"up_q", w->up_q, E * I * qb(H)},
-                      {"up_s", w->up_s, E * I * sb(H)},
-                      {"down_q", w->down_q, E * H * qb(I)},
-                      {"down_s", w->down_s, E * H * sb(I)}};
+                      {"gate_q", w->gate_q, Er * I * qb(H)},
+                      {"gate_s", w->gate_s, Er * I * sb(H)},
+                      {"up_q", w->up_q, Er * I * qb(H)},
+                      {"up_s", w->up_s, Er * I * sb(H)},
+                      {"down_q", w->down_q, Er * H * qb(I)},
+                      {"down_s", w->down_s, Er * H * sb(I)}};
   for (const A& x : routed)
     if (const char* m = check_extent(x.p, x.bytes, device)) {
       *which = x.name;
@@ -418,6 +421,14 @@ size_t moe_workspace_bytes(const moe_config_t* cfg) {
 
 moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
                               moe_layer_t** out) {
+  if (!cfg || check_config(cfg)) return moe::layer_create_slots(cfg, w, 0, out);
+  return moe::layer_create_slots(cfg, w, cfg->n_experts, out);
+}
+
+}  // extern "C"
+
+moe_status_t moe::layer_create_slots(const moe_config_t* cfg, const moe_weights_t* w,
+                                     int routed_experts, moe_layer_t** out) {
   if (!out) {
     set_err(nullptr, "out is NULL");
     return MOE_ERR_INVALID_ARG;
@@ -461,7 +472,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
   // (after the workspace allocation, which has made the device's context
   // current on this thread for the driver query)
   const char* which = "";
-  if (const char* m = check_weight_memory(cfg, w, h->device, &which)) {
+  if (const char* m = check_weight_memory(cfg, w, static_cast<size_t>(routed_experts),
+                                          h->device, &which)) {
     set_err(nullptr, "weight array %s %s", which, m);
     cudaFree(h->ws_base);
     delete h;
@@ -477,14 +489,19 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* w,
     delete h;
     return MOE_ERR_CUDA;
   }
-  // tensor-core path: TMA tensor maps over the weights and the f16 rows
-  h->tc = moe::tc_path_ok(h->sh) ? moe::tc_create_maps(h->w, h->sh, h->ws, cfg->max_tokens)
-                                 : nullptr;
-  // single-token tensor-core kernel: TMA tensor maps over the weights
-  h->dm = moe::dm_shape_ok(h->sh) ? moe::dm_create_maps(h->w, h->sh) : nullptr;
+  // tensor-core path: TMA tensor maps over the weights and the f16 rows;
+  // single-token tensor-core kernel: TMA tensor maps over the weights (not
+  // for the expert tier's slots, which only the SIMT batch kernels read)
+  const bool all = routed_experts == cfg->n_experts;
+  h->tc = all && moe::tc_path_ok(h->sh)
+              ? moe::tc_create_maps(h->w, h->sh, h->ws, cfg->max_tokens)
+              : nullptr;
+  h->dm = all && moe::dm_shape_ok(h->sh) ? moe::dm_create_maps(h->w, h->sh) : nullptr;
   *out = h;
   return MOE_OK;
 }
+
+extern "C" {
 
 // x or y of a call as the kernels address it: device (or managed) memory as
 // it is, pinned host memory through its device mapping (the kernels then read
@@ -509,6 +526,52 @@ static moe_status_t resolve_io(moe_layer_t* h, const void* p, const void** out, 
              "address space", what);
   return MOE_ERR_INVALID_ARG;
 }
+
+}  // extern "C"
+
+moe_status_t moe::layer_check_call(moe_layer* h, const void** x, moe_dtype_t dtype, int T,
+                                   float** y, const float* rms_gamma, int accumulate,
+                                   const moe_plan_t* plan_out, bool route_only) {
+  moe_status_t st = check_call(h, *x, dtype, T, rms_gamma);
+  if (st != MOE_OK || T == 0) return st;
+  if ((st = check_plan(h, plan_out)) != MOE_OK) return st;
+  if (route_only) return resolve_io(h, *x, x, "x");
+  if (!*y || !aligned16(*y)) {
+    set_err(h, "y must be a non-NULL 16-byte aligned device pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  const size_t H = h->cfg.hidden;
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(*x);
+  const uintptr_t xe = xb + static_cast<size_t>(T) * H * (dtype == MOE_BF16 ? 2 : 4);
+  const uintptr_t yb = reinterpret_cast<uintptr_t>(*y);
+  const uintptr_t ye = yb + static_cast<size_t>(T) * H * 4;
+  if (xb < ye && yb < xe) {
+    const bool residual_form =
+        dtype == MOE_F32 && accumulate && rms_gamma != nullptr && xb == yb;
+    if (!residual_form) {
+      set_err(h, "x and y overlap; only the in-place residual form (f32, accumulate, "
+                 "rms_gamma, y == x) is allowed");
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if ((st = resolve_io(h, *x, x, "x")) != MOE_OK) return st;
+  const void* yd = nullptr;
+  if ((st = resolve_io(h, *y, &yd, "y")) != MOE_OK) return st;
+  *y = static_cast<float*>(const_cast<void*>(yd));
+  return MOE_OK;
+}
+
+cudaError_t moe::layer_route(moe_layer* h, const void* x, moe_dtype_t dt, int T,
+                             const float* gamma, float eps, cudaStream_t s) {
+  Tracer none;
+  return run_route(h, x, dt, T, gamma, eps, s, none);
+}
+
+cudaError_t moe::layer_copy_plan(moe_layer* h, int T, const moe_plan_t* p, cudaStream_t s) {
+  return copy_plan(h, T, p, s);
+}
+
+extern "C" {
 
 moe_status_t moe_route(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T,
                        const float* rms_gamma, float rms_eps, moe_plan_t* plan_out,
@@ -536,33 +599,9 @@ moe_status_t moe_forward(moe_layer_t* h, const void* x, moe_dtype_t dtype, int T
     set_err(nullptr, "handle is NULL");
     return MOE_ERR_INVALID_ARG;
   }
-  moe_status_t st = check_call(h, x, dtype, T, rms_gamma);
+  moe_status_t st =
+      moe::layer_check_call(h, &x, dtype, T, &y, rms_gamma, accumulate, plan_out, false);
   if (st != MOE_OK || T == 0) return st;
-  if ((st = check_plan(h, plan_out)) != MOE_OK) return st;
-  if (!y || !aligned16(y)) {
-    set_err(h, "y must be a non-NULL 16-byte aligned device pointer");
-    return MOE_ERR_INVALID_ARG;
-  }
-  const size_t H = h->cfg.hidden;
-  const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
-  const uintptr_t xe = xb + static_cast<size_t>(T) * H * (dtype == MOE_BF16 ? 2 : 4);
-  const uintptr_t yb = reinterpret_cast<uintptr_t>(y);
-  const uintptr_t ye = yb + static_cast<size_t>(T) * H * 4;
-  if (xb < ye && yb < xe) {
-    const bool residual_form =
-        dtype == MOE_F32 && accumulate && rms_gamma != nullptr && xb == yb;
-    if (!residual_form) {
-      set_err(h, "x and y overlap; only the in-place residual form (f32, accumulate, "
-                 "rms_gamma, y == x) is allowed");
-      return MOE_ERR_INVALID_ARG;
-    }
-  }
-  if ((st = resolve_io(h, x, &x, "x")) != MOE_OK) return st;
-  {
-    const void* yd = nullptr;
-    if ((st = resolve_io(h, y, &yd, "y")) != MOE_OK) return st;
-    y = static_cast<float*>(const_cast<void*>(yd));
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Tracer tr;
   tr.start(h, s);

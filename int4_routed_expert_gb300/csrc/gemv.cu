@@ -19,7 +19,13 @@
 // Every expert format runs here (N2: symmetric int4/int8, per-row or grouped
 // scales): packed offset-binary int4 or signed int8 weights, one fp16 scale
 // per 32 values or one per row.
+//
+// The expert tier (tier.cu) runs the same kernels with a slot table: each
+// routed expert reads its weights from the HBM slot the table names, and a
+// launch takes only the experts of one phase (resident ones first, loaded
+// ones once their copies have landed).
 #include "moe_internal.cuh"
+#include "tier_internal.cuh"
 
 namespace moe {
 namespace {
@@ -242,9 +248,25 @@ __device__ inline void stage_rows(float* xs, const float* src, size_t src_stride
   }
 }
 
+// Whether a run belongs to this launch, and the weight index of its expert.
+// phase < 0: every run, expert e at index e.  Otherwise the routed run of
+// expert e belongs to phase slot_tab[e] >> kSlotPhaseShift and reads slot
+// slot_tab[e] & mask; the shared expert belongs to phase 0.  The same for
+// every thread of the CTA.
+__device__ __forceinline__ bool run_in_phase(int e, const int32_t* slot_tab, int phase,
+                                             int& slot) {
+  slot = e;
+  if (phase < 0) return true;
+  if (e < 0) return phase == 0;
+  const int v = __ldg(slot_tab + e);
+  slot = v & ((1 << kSlotPhaseShift) - 1);
+  return (v >> kSlotPhaseShift) == phase;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kWarps * 32)
-gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
+gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws,
+               const int32_t* __restrict__ slot_tab, int phase) {
   extern __shared__ float xs[];
   __shared__ Run runs[kNT];
   __shared__ int n_runs;
@@ -255,6 +277,8 @@ gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
   for (int ri = 0; ri < n_runs; ++ri) {
     const Run& run = runs[ri];
     const bool shared = run.e < 0;
+    int slot = run.e;
+    if (!run_in_phase(run.e, slot_tab, phase, slot)) continue;
     const int I = shared ? sh.Is : sh.I;
     const int r0 = blockIdx.x * kRows;
     if (r0 >= I) continue;
@@ -262,8 +286,8 @@ gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
     stage_rows(xs, ws.xf, sh.H, run.tok, run.n, sh.H);
     __syncthreads();
     const RowFmt f = row_fmt(sh, sh.H);
-    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * I * f.qb;
-    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * I * f.ns;
+    const size_t eq = shared ? 0 : static_cast<size_t>(slot) * I * f.qb;
+    const size_t es = shared ? 0 : static_cast<size_t>(slot) * I * f.ns;
     const uint8_t* gq = (shared ? w.sh_gate_q : w.gate_q) + eq;
     const uint16_t* gs = (shared ? w.sh_gate_s : w.gate_s) + es;
     const uint8_t* uq = (shared ? w.sh_up_q : w.up_q) + eq;
@@ -280,7 +304,8 @@ gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
 
 template <int FMT>
 __global__ void __launch_bounds__(kWarps * 32)
-down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
+down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws,
+            const int32_t* __restrict__ slot_tab, int phase) {
   extern __shared__ float hs[];
   __shared__ Run runs[kNT];
   __shared__ int n_runs;
@@ -292,13 +317,15 @@ down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws) {
   for (int ri = 0; ri < n_runs; ++ri) {
     const Run& run = runs[ri];
     const bool shared = run.e < 0;
+    int slot = run.e;
+    if (!run_in_phase(run.e, slot_tab, phase, slot)) continue;
     const int I = shared ? sh.Is : sh.I;
     __syncthreads();
     stage_rows(hs, ws.hbuf, ws.hstride, run.row, run.n, I);
     __syncthreads();
     const RowFmt f = row_fmt(sh, I);
-    const size_t eq = shared ? 0 : static_cast<size_t>(run.e) * sh.H * f.qb;
-    const size_t es = shared ? 0 : static_cast<size_t>(run.e) * sh.H * f.ns;
+    const size_t eq = shared ? 0 : static_cast<size_t>(slot) * sh.H * f.qb;
+    const size_t es = shared ? 0 : static_cast<size_t>(slot) * sh.H * f.ns;
     const uint8_t* dq = (shared ? w.sh_down_q : w.down_q) + eq;
     const uint16_t* ds = (shared ? w.sh_down_s : w.down_s) + es;
     switch (run.n) {
@@ -362,8 +389,9 @@ int tiles_y(const Shape& sh, int T) {
 
 }  // namespace
 
-cudaError_t launch_gate_up(const moe_weights_t& w, const Shape& sh, int T, const Workspace& ws,
-                           cudaStream_t s) {
+cudaError_t launch_gate_up_slots(const moe_weights_t& w, const Shape& sh, int T,
+                                 const Workspace& ws, const int32_t* slot_tab, int phase,
+                                 cudaStream_t s) {
   const int Imax = sh.n_shared ? max(sh.I, sh.Is) : sh.I;
   const size_t smem = static_cast<size_t>(kNT) * (sh.H / 32) * kGS * sizeof(float);
   auto kern = sh.wfmt == MOE_W_INT8 ? gate_up_kernel<MOE_W_INT8> : gate_up_kernel<MOE_W_INT4>;
@@ -371,12 +399,12 @@ cudaError_t launch_gate_up(const moe_weights_t& w, const Shape& sh, int T, const
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
   const dim3 grid((Imax + kRows - 1) / kRows, min(nt, 65535));
-  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
+  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws, slot_tab, phase);
   return cudaGetLastError();
 }
 
-cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T, const Workspace& ws,
-                        cudaStream_t s) {
+cudaError_t launch_down_slots(const moe_weights_t& w, const Shape& sh, int T, const Workspace& ws,
+                              const int32_t* slot_tab, int phase, cudaStream_t s) {
   const int Imax = sh.n_shared ? max(sh.I, sh.Is) : sh.I;
   const size_t smem = static_cast<size_t>(kNT) * (Imax / 32) * kGS * sizeof(float);
   auto kern = sh.wfmt == MOE_W_INT8 ? down_kernel<MOE_W_INT8> : down_kernel<MOE_W_INT4>;
@@ -384,8 +412,18 @@ cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T, const Wo
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
   const dim3 grid((sh.H + kRows - 1) / kRows, min(nt, 65535));
-  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws);
+  kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws, slot_tab, phase);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gate_up(const moe_weights_t& w, const Shape& sh, int T, const Workspace& ws,
+                           cudaStream_t s) {
+  return launch_gate_up_slots(w, sh, T, ws, nullptr, -1, s);
+}
+
+cudaError_t launch_down(const moe_weights_t& w, const Shape& sh, int T, const Workspace& ws,
+                        cudaStream_t s) {
+  return launch_down_slots(w, sh, T, ws, nullptr, -1, s);
 }
 
 cudaError_t launch_combine(const Shape& sh, int T, const Workspace& ws, float* y,

@@ -8,9 +8,12 @@ Low-level functions mirror include/moe.h one to one:
     moe_layer_create, moe_route, moe_forward, moe_destroy, moe_last_error,
     moe_workspace_bytes, moe_trace_enable, moe_trace_read,
     moe_trace_phase_name, moe_device_status, moe_selftest_bounded_wait,
-    moe_selftest_desync
+    moe_selftest_desync, moe_route_noalloc, the expert slot cache
+    (moe_slot_cache_*) and the expert tier (moe_tier_*)
 ``MoELayer`` wraps a handle around torch tensors (device memory and streams
-only) for the tests and the benchmark.
+only) for the tests and the benchmark; ``ExpertTier`` does the same for an
+expert tier (routed experts in pinned host memory, a bounded set in HBM) and
+``SlotCache`` for the tier's host-side residency policy.
 """
 from __future__ import annotations
 
@@ -61,10 +64,28 @@ class moe_plan_t(C.Structure):
         "topk_ids", "topk_w", "counts", "offsets", "perm", "active", "n_active")]
 
 
+class moe_tier_config_t(C.Structure):
+    _fields_ = [("n_slots", C.c_int), ("n_pinned", C.c_int)]
+
+
+class moe_slot_cache_stats_t(C.Structure):
+    _fields_ = [("hits_pinned", C.c_uint64), ("hits_lru", C.c_uint64), ("misses", C.c_uint64),
+                ("loads", C.c_uint64), ("evictions", C.c_uint64), ("n_resident", C.c_int32),
+                ("n_pinned", C.c_int32)]
+
+
+# kinds of an admitted expert (moe_slot_cache_admit)
+SLOT_HIT_PINNED, SLOT_HIT_LRU, SLOT_LOAD = 0, 1, 2
+
 EXPORTED = ("moe_layer_create", "moe_route", "moe_forward", "moe_destroy",
             "moe_last_error", "moe_workspace_bytes", "moe_trace_enable", "moe_trace_read",
             "moe_trace_phase_name", "moe_device_status", "moe_route_noalloc",
-            "moe_selftest_bounded_wait", "moe_selftest_desync")
+            "moe_selftest_bounded_wait", "moe_selftest_desync",
+            "moe_slot_cache_create", "moe_slot_cache_admit", "moe_slot_cache_prefetch",
+            "moe_slot_cache_pin", "moe_slot_cache_repin", "moe_slot_cache_query",
+            "moe_slot_cache_destroy", "moe_tier_create", "moe_tier_forward",
+            "moe_tier_prefetch", "moe_tier_prefetch_routed", "moe_tier_pin", "moe_tier_repin",
+            "moe_tier_query", "moe_tier_last_error", "moe_tier_destroy")
 
 _lib = None
 
@@ -111,6 +132,42 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.moe_route_noalloc.argtypes = [C.POINTER(moe_config_t), C.c_void_p, C.c_void_p, C.c_void_p,
                                     C.c_int, C.c_int, C.c_void_p, C.c_float,
                                     C.POINTER(moe_plan_t), C.c_void_p]
+    i32p = C.POINTER(C.c_int32)
+    u64p = C.POINTER(C.c_uint64)
+    L.moe_slot_cache_create.restype = C.c_int
+    L.moe_slot_cache_create.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int,
+                                        C.POINTER(C.c_void_p)]
+    for fn in ("moe_slot_cache_admit", "moe_slot_cache_prefetch", "moe_slot_cache_pin"):
+        getattr(L, fn).restype = C.c_int
+        getattr(L, fn).argtypes = [C.c_void_p, i32p, C.c_int, i32p, i32p]
+    L.moe_slot_cache_repin.restype = C.c_int
+    L.moe_slot_cache_repin.argtypes = [C.c_void_p, C.c_int]
+    L.moe_slot_cache_query.restype = C.c_int
+    L.moe_slot_cache_query.argtypes = [C.c_void_p, C.POINTER(moe_slot_cache_stats_t), i32p,
+                                       u64p]
+    L.moe_slot_cache_destroy.restype = None
+    L.moe_slot_cache_destroy.argtypes = [C.c_void_p]
+    L.moe_tier_create.restype = C.c_int
+    L.moe_tier_create.argtypes = [C.POINTER(moe_config_t), C.POINTER(moe_weights_t),
+                                  C.POINTER(moe_tier_config_t), C.POINTER(C.c_void_p)]
+    L.moe_tier_forward.restype = C.c_int
+    L.moe_tier_forward.argtypes = L.moe_forward.argtypes
+    L.moe_tier_prefetch.restype = C.c_int
+    L.moe_tier_prefetch.argtypes = [C.c_void_p, i32p, C.c_int]
+    L.moe_tier_prefetch_routed.restype = C.c_int
+    L.moe_tier_prefetch_routed.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
+                                           C.c_float, C.c_void_p]
+    L.moe_tier_pin.restype = C.c_int
+    L.moe_tier_pin.argtypes = [C.c_void_p, i32p, C.c_int]
+    L.moe_tier_repin.restype = C.c_int
+    L.moe_tier_repin.argtypes = [C.c_void_p, C.c_int, C.POINTER(C.c_int)]
+    L.moe_tier_query.restype = C.c_int
+    L.moe_tier_query.argtypes = [C.c_void_p, C.POINTER(moe_slot_cache_stats_t), i32p, u64p,
+                                 u64p]
+    L.moe_tier_last_error.restype = C.c_char_p
+    L.moe_tier_last_error.argtypes = [C.c_void_p]
+    L.moe_tier_destroy.restype = None
+    L.moe_tier_destroy.argtypes = [C.c_void_p]
     _lib = L
     return L
 
@@ -249,27 +306,11 @@ class Plan:
                                  f"with at least {n} elements")
 
 
-class MoELayer:
-    """Handle + the tensors it borrows.  torch supplies memory and streams."""
+class _TensorIO:
+    """Argument checks shared by the torch wrappers (shape, device, dtype)."""
 
-    def __init__(self, layer_inputs, max_tokens: int):
-        self.inputs = layer_inputs  # keeps the weights alive
-        self.shape = layer_inputs.shape
-        self.device = layer_inputs.router_w.device
-        self.max_tokens = max_tokens
-        self.cfg = config_for(self.shape, max_tokens)
-        self.h = moe_layer_create(self.cfg, weights_for(layer_inputs))
-
-    def close(self):
-        if self.h:
-            moe_destroy(self.h)
-            self.h = None
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
+    shape = None
+    device = None
 
     @staticmethod
     def _dtype(x) -> int:
@@ -311,6 +352,42 @@ class MoELayer:
         s = stream if stream is not None else torch.cuda.current_stream()
         return s.cuda_stream
 
+    def _forward_args(self, x, y, gamma, plan):
+        """Checks forward's tensors; returns (T, y, plan struct or None)."""
+        import torch
+        T = self._check_x(x)
+        if y is None:
+            y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=self.device)
+        self._check_vec(y, "y", T, self.device, host_ok=True)
+        if gamma is not None:
+            self._check_vec(gamma, "gamma", 1, self.device)
+        if plan is not None:
+            plan.check(T, self.shape.top_k, self.shape.n_experts, self.device)
+        return T, y, (plan.c() if plan is not None else None)
+
+
+class MoELayer(_TensorIO):
+    """Handle + the tensors it borrows.  torch supplies memory and streams."""
+
+    def __init__(self, layer_inputs, max_tokens: int):
+        self.inputs = layer_inputs  # keeps the weights alive
+        self.shape = layer_inputs.shape
+        self.device = layer_inputs.router_w.device
+        self.max_tokens = max_tokens
+        self.cfg = config_for(self.shape, max_tokens)
+        self.h = moe_layer_create(self.cfg, weights_for(layer_inputs))
+
+    def close(self):
+        if self.h:
+            moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
     def route(self, x, gamma=None, eps: float = 1e-5, plan: Plan | None = None,
               stream=None) -> Plan:
         T = self._check_x(x)
@@ -326,17 +403,169 @@ class MoELayer:
 
     def forward(self, x, y=None, gamma=None, eps: float = 1e-5, accumulate: bool = False,
                 plan: Plan | None = None, stream=None):
-        import torch
-        T = self._check_x(x)
-        if y is None:
-            y = torch.empty(T, self.shape.hidden, dtype=torch.float32, device=self.device)
-        self._check_vec(y, "y", T, self.device, host_ok=True)
-        if gamma is not None:
-            self._check_vec(gamma, "gamma", 1, self.device)
-        if plan is not None:
-            plan.check(T, self.shape.top_k, self.shape.n_experts, self.device)
-        pc = plan.c() if plan is not None else None
+        T, y, pc = self._forward_args(x, y, gamma, plan)
         moe_forward(self.h, x.data_ptr(), self._dtype(x), T, y.data_ptr(),
                     gamma.data_ptr() if gamma is not None else None, eps,
                     1 if accumulate else 0, pc, self._stream(stream))
         return y
+
+
+# ------------------------------------------------------------ expert tier --
+
+ROUTED_ARRAYS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+
+
+def _i32(ids):
+    """ctypes int32 array of a sequence of expert ids, and its length."""
+    v = [int(e) for e in ids]
+    return (C.c_int32 * max(1, len(v)))(*v), len(v)
+
+
+def _stats_dict(st: moe_slot_cache_stats_t) -> dict:
+    return {n: int(getattr(st, n)) for n, _ in moe_slot_cache_stats_t._fields_}
+
+
+class SlotCache:
+    """The expert tier's residency policy on the host (moe_slot_cache_*)."""
+
+    def __init__(self, n_experts: int, n_slots: int, n_pinned: int, call_slots: int):
+        self.n_experts = n_experts
+        h = C.c_void_p()
+        _check(load().moe_slot_cache_create(n_experts, n_slots, n_pinned, call_slots,
+                                            C.byref(h)))
+        self.h = h
+
+    def _op(self, fn, ids):
+        a, n = _i32(ids)
+        slot = (C.c_int32 * max(1, n))()
+        kind = (C.c_int32 * max(1, n))()
+        _check(fn(self.h, a, n, slot, kind))
+        return list(slot[:n]), list(kind[:n])
+
+    def admit(self, ids):
+        """-> (slots, kinds) of one call's distinct experts."""
+        return self._op(load().moe_slot_cache_admit, ids)
+
+    def prefetch(self, ids):
+        return self._op(load().moe_slot_cache_prefetch, ids)
+
+    def pin(self, ids):
+        return self._op(load().moe_slot_cache_pin, ids)
+
+    def repin(self, max_swaps: int) -> int:
+        r = load().moe_slot_cache_repin(self.h, max_swaps)
+        if r < 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, "moe_slot_cache_repin: bad arguments")
+        return r
+
+    def query(self):
+        """-> (counters, slot_of [E] (-(slot+2) when pinned, -1 absent), uses [E])."""
+        st = moe_slot_cache_stats_t()
+        slot_of = (C.c_int32 * self.n_experts)()
+        uses = (C.c_uint64 * self.n_experts)()
+        _check(load().moe_slot_cache_query(self.h, C.byref(st), slot_of, uses))
+        return _stats_dict(st), list(slot_of), list(uses)
+
+    def close(self):
+        if self.h:
+            load().moe_slot_cache_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class ExpertTier(_TensorIO):
+    """Expert tier (moe_tier_*): the routed experts of ``layer_inputs`` are
+    copied to pinned host memory (the slower tier); ``n_slots`` of them are
+    held in HBM at a time.  The router and the shared expert stay on the
+    device.  ``drop_device_routed`` releases the device copies of the routed
+    arrays from ``layer_inputs`` afterwards."""
+
+    def __init__(self, layer_inputs, max_tokens: int, n_slots: int, n_pinned: int = 0,
+                 drop_device_routed: bool = False):
+        import torch
+        L = layer_inputs
+        self.shape = L.shape
+        self.device = L.router_w.device
+        self.max_tokens = max_tokens
+        self.cfg = config_for(self.shape, max_tokens)
+        self.host = {}
+        for n in ROUTED_ARRAYS:
+            t = getattr(L, n)
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            self.host[n] = h
+        w = weights_for(L)
+        for n in ROUTED_ARRAYS:
+            setattr(w, n, self.host[n].data_ptr())
+        if drop_device_routed:
+            for n in ROUTED_ARRAYS:
+                setattr(L, n, None)
+        self.inputs = L  # keeps the router and shared-expert tensors alive
+        h = C.c_void_p()
+        tc = moe_tier_config_t(n_slots, n_pinned)
+        st = load().moe_tier_create(C.byref(self.cfg), C.byref(w), C.byref(tc), C.byref(h))
+        if st != MOE_OK:
+            raise MoeError(st, moe_last_error(None))
+        self.h = h
+
+    def _check(self, st):
+        if st != MOE_OK:
+            raise MoeError(st, (load().moe_tier_last_error(self.h) or b"").decode())
+
+    def forward(self, x, y=None, gamma=None, eps: float = 1e-5, accumulate: bool = False,
+                plan: Plan | None = None, stream=None):
+        T, y, pc = self._forward_args(x, y, gamma, plan)
+        self._check(load().moe_tier_forward(
+            self.h, x.data_ptr(), self._dtype(x), T, y.data_ptr(),
+            gamma.data_ptr() if gamma is not None else None, eps, 1 if accumulate else 0,
+            C.byref(pc) if pc is not None else None, self._stream(stream)))
+        return y
+
+    def prefetch(self, ids) -> None:
+        a, n = _i32(ids)
+        self._check(load().moe_tier_prefetch(self.h, a, n))
+
+    def prefetch_routed(self, x, gamma=None, eps: float = 1e-5, stream=None) -> None:
+        T = self._check_x(x)
+        if gamma is not None:
+            self._check_vec(gamma, "gamma", 1, self.device)
+        self._check(load().moe_tier_prefetch_routed(
+            self.h, x.data_ptr(), self._dtype(x), T,
+            gamma.data_ptr() if gamma is not None else None, eps, self._stream(stream)))
+
+    def pin(self, ids) -> None:
+        a, n = _i32(ids)
+        self._check(load().moe_tier_pin(self.h, a, n))
+
+    def repin(self, max_swaps: int) -> int:
+        c = C.c_int(0)
+        self._check(load().moe_tier_repin(self.h, max_swaps, C.byref(c)))
+        return c.value
+
+    def query(self):
+        """-> (counters incl. h2d_bytes, slot_of [E], uses [E])."""
+        E = self.shape.n_experts
+        st = moe_slot_cache_stats_t()
+        slot_of = (C.c_int32 * E)()
+        uses = (C.c_uint64 * E)()
+        h2d = C.c_uint64(0)
+        self._check(load().moe_tier_query(self.h, C.byref(st), slot_of, uses, C.byref(h2d)))
+        d = _stats_dict(st)
+        d["h2d_bytes"] = int(h2d.value)
+        return d, list(slot_of), list(uses)
+
+    def close(self):
+        if self.h:
+            load().moe_tier_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

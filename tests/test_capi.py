@@ -190,3 +190,24 @@ def test_other_formats_are_accepted(m, fmt):
     lib = m.load()
     assert lib.moe_workspace_bytes(C.byref(_cfg(m, **fmt))) == \
         lib.moe_workspace_bytes(C.byref(_cfg(m)))
+
+
+def test_tier_create_validates_before_any_cuda_call(m):
+    """The expert tier's argument checks run on the host: NULL arguments,
+    a bad geometry, and slot counts that cannot hold one call's union."""
+    lib = m.load()
+    h = C.c_void_p()
+    w = _fake_weights(m)
+    tc = m.moe.moe_tier_config_t
+    assert lib.moe_tier_create(None, C.byref(w), C.byref(tc(8, 0)), C.byref(h)) == -1
+    assert lib.moe_tier_create(C.byref(_cfg(m, hidden=300)), C.byref(w), C.byref(tc(8, 0)),
+                               C.byref(h)) == -2
+    # max_tokens 8 x top-4 over 16 experts: a union may hold all 16
+    for slots, pinned in ((0, 0), (17, 0), (15, 0), (16, 1), (16, -1)):
+        st = lib.moe_tier_create(C.byref(_cfg(m)), C.byref(w), C.byref(tc(slots, pinned)),
+                                 C.byref(h))
+        assert st == -1 and not h.value, (slots, pinned)
+        assert b"n_slots" in lib.moe_last_error(None)
+    assert lib.moe_tier_forward(None, None, 0, 1, None, None, 0.0, 0, None, None) == -1
+    assert lib.moe_tier_repin(None, 1, None) == -1
+    lib.moe_tier_destroy(None)
