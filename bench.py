@@ -858,7 +858,10 @@ def main():
             swl = make_workload(sub)
             subs[sub] = measure(args, swl, dev, world, 1, args.warmup, clocks,
                                 min_timed_s=SUB_MIN_TIMED_S)
-        subs["glm_decode_tier"] = measure_tier(dev, clocks, args.warmup)
+        try:
+            subs["glm_decode_tier"] = measure_tier(dev, clocks, args.warmup)
+        except Exception as e:  # the headline line must still be printed
+            subs["glm_decode_tier"] = {"error": f"{type(e).__name__}: {e}"}
     clocks.stop()
 
     if rank == 0:
