@@ -14,7 +14,8 @@
 //
 // A CTA owns a tile of kNT consecutive plan positions (or kNT tokens of the
 // shared expert) and 64 output rows; positions of one expert inside the tile
-// form one run that streams each weight row once for all of its tokens.
+// form one run that streams each weight row once for all of its tokens.  For
+// T <= 4 the runs of a tile are spread over blockIdx.z, one CTA each.
 //
 // Every expert format runs here (N2: symmetric int4/int8, per-row or grouped
 // scales): packed offset-binary int4 or signed int8 weights, one fp16 scale
@@ -274,7 +275,7 @@ gate_up_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws,
   __syncthreads();
   if (threadIdx.x == 0) n_runs = tile_runs(ws, T, sh.k, y, runs);
   __syncthreads();
-  for (int ri = 0; ri < n_runs; ++ri) {
+  for (int ri = blockIdx.z; ri < n_runs; ri += gridDim.z) {
     const Run& run = runs[ri];
     const bool shared = run.e < 0;
     int slot = run.e;
@@ -314,7 +315,7 @@ down_kernel(moe_weights_t w, Shape sh, int T, int n_tiles, Workspace ws,
   __syncthreads();
   if (threadIdx.x == 0) n_runs = tile_runs(ws, T, sh.k, y, runs);
   __syncthreads();
-  for (int ri = 0; ri < n_runs; ++ri) {
+  for (int ri = blockIdx.z; ri < n_runs; ri += gridDim.z) {
     const Run& run = runs[ri];
     const bool shared = run.e < 0;
     int slot = run.e;
@@ -383,6 +384,11 @@ cudaError_t set_smem(const void* fn, size_t bytes) {
                               static_cast<int>(bytes));
 }
 
+// Small batches (T <= 4): the runs of a tile (distinct experts, at most kNT)
+// go to kNT CTAs (blockIdx.z) instead of one CTA in turn, so that a call's
+// few experts stream in parallel.  Larger batches keep one CTA per tile.
+int runs_z(int T) { return T <= 4 ? kNT : 1; }
+
 int tiles_y(const Shape& sh, int T) {
   return (T * sh.k + kNT - 1) / kNT + (sh.n_shared ? (T + kNT - 1) / kNT : 0);
 }
@@ -398,7 +404,7 @@ cudaError_t launch_gate_up_slots(const moe_weights_t& w, const Shape& sh, int T,
   cudaError_t e = set_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
-  const dim3 grid((Imax + kRows - 1) / kRows, min(nt, 65535));
+  const dim3 grid((Imax + kRows - 1) / kRows, min(nt, 65535), runs_z(T));
   kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws, slot_tab, phase);
   return cudaGetLastError();
 }
@@ -411,7 +417,7 @@ cudaError_t launch_down_slots(const moe_weights_t& w, const Shape& sh, int T, co
   cudaError_t e = set_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int nt = tiles_y(sh, T);
-  const dim3 grid((sh.H + kRows - 1) / kRows, min(nt, 65535));
+  const dim3 grid((sh.H + kRows - 1) / kRows, min(nt, 65535), runs_z(T));
   kern<<<grid, kWarps * 32, smem, s>>>(w, sh, T, nt, ws, slot_tab, phase);
   return cudaGetLastError();
 }
