@@ -400,6 +400,9 @@ void moe_slot_cache_destroy(moe_slot_cache_t* c);
  *   query; *h2d_bytes (may be NULL) = expert bytes copied into HBM so far.
  * moe_tier_last_error(t): the tier's last message (moe_last_error(NULL) for
  *   failures of moe_tier_create).
+ * A CUDA failure inside forward, prefetch or pin (MOE_ERR_CUDA) leaves the
+ *   tier unusable: the slots may not hold what its cache records, so every
+ *   later forward, prefetch and pin returns MOE_ERR_CUDA; destroy it.
  * moe_tier_destroy(t): waits for the tier's work and frees it (NULL is
  *   ignored). */
 typedef struct moe_tier moe_tier_t;

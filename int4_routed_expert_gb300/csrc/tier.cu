@@ -56,6 +56,10 @@ struct moe_tier {
   int32_t* h_tab = nullptr;    // pinned host [E]: slot table staging
   int32_t* d_tab = nullptr;    // device [E]: slot table of the current call
   uint64_t h2d = 0;            // expert bytes copied into HBM
+  // set by a failed CUDA call after the slot cache had taken its decisions:
+  // the slots may no longer hold what the cache says, so every later call
+  // is refused
+  bool broken = false;
   char err[512] = {};
 };
 
@@ -76,7 +80,15 @@ void terr(moe_tier* t, const char* fmt, ...) {
 
 moe_status_t tcuda(moe_tier* t, cudaError_t e, const char* what) {
   terr(t, "%s: %s", what, cudaGetErrorString(e));
+  if (t) t->broken = true;
   return MOE_ERR_CUDA;
+}
+
+// Refuses calls on a tier that a failed CUDA call left inconsistent.
+bool refuse_broken(moe_tier* t, const char* what) {
+  if (!t->broken) return false;
+  terr(t, "%s: the tier is unusable after an earlier CUDA error", what);
+  return true;
 }
 
 void free_tier(moe_tier* t) {
@@ -296,6 +308,7 @@ moe_status_t moe_tier_forward(moe_tier_t* t, const void* x, moe_dtype_t dtype, i
     moe::set_thread_error("moe_tier_forward: tier is NULL");
     return MOE_ERR_INVALID_ARG;
   }
+  if (refuse_broken(t, "moe_tier_forward")) return MOE_ERR_CUDA;
   moe_status_t st =
       moe::layer_check_call(t->L, &x, dtype, T, &y, rms_gamma, accumulate, plan_out, false);
   if (st != MOE_OK) {
@@ -355,6 +368,7 @@ moe_status_t moe_tier_prefetch(moe_tier_t* t, const int32_t* ids, int n) {
     moe::set_thread_error("moe_tier_prefetch: tier is NULL");
     return MOE_ERR_INVALID_ARG;
   }
+  if (refuse_broken(t, "moe_tier_prefetch")) return MOE_ERR_CUDA;
   refresh_done(t);
   return place_and_load(t, ids, n, 1, "moe_tier_prefetch");
 }
@@ -365,6 +379,7 @@ moe_status_t moe_tier_prefetch_routed(moe_tier_t* t, const void* x, moe_dtype_t 
     moe::set_thread_error("moe_tier_prefetch_routed: tier is NULL");
     return MOE_ERR_INVALID_ARG;
   }
+  if (refuse_broken(t, "moe_tier_prefetch_routed")) return MOE_ERR_CUDA;
   moe_status_t st =
       moe::layer_check_call(t->L, &x, dtype, T, nullptr, rms_gamma, 0, nullptr, true);
   if (st != MOE_OK) {
@@ -384,6 +399,7 @@ moe_status_t moe_tier_pin(moe_tier_t* t, const int32_t* ids, int n) {
     moe::set_thread_error("moe_tier_pin: tier is NULL");
     return MOE_ERR_INVALID_ARG;
   }
+  if (refuse_broken(t, "moe_tier_pin")) return MOE_ERR_CUDA;
   refresh_done(t);
   return place_and_load(t, ids, n, 2, "moe_tier_pin");
 }
