@@ -46,7 +46,8 @@ struct moe_tier {
   size_t mat_bytes[kMats] = {};          // bytes of one expert's matrix
   void* pool = nullptr;
   cudaStream_t copy_s = nullptr;
-  cudaEvent_t batch_ev[kRing] = {};
+  cudaEvent_t gu_ev[kRing] = {};     // a batch's gate/up copies have landed
+  cudaEvent_t batch_ev[kRing] = {};  // all of a batch's copies have landed
   cudaEvent_t call_done = nullptr;  // recorded after the last call's kernels
   bool any_call = false;
   long long n_batches = 0;     // copy batches issued
@@ -97,6 +98,8 @@ void free_tier(moe_tier* t) {
   if (t->L) moe_destroy(t->L);  // waits for the device
   for (cudaEvent_t& e : t->batch_ev)
     if (e) cudaEventDestroy(e);
+  for (cudaEvent_t& e : t->gu_ev)
+    if (e) cudaEventDestroy(e);
   if (t->call_done) cudaEventDestroy(t->call_done);
   if (t->copy_s) cudaStreamDestroy(t->copy_s);
   cudaFree(t->pool);
@@ -120,8 +123,11 @@ void refresh_done(moe_tier* t) {
 }
 
 // Copies the experts placed with kind kSlotLoad into their slots as one
-// batch on the copy stream; returns the batch number in *batch (-1 when
-// nothing was loaded).
+// batch on the copy stream, gate/up matrices of every load first (event
+// gu_ev), then the down matrices (event batch_ev), so that the gate/up
+// kernels of the loaded experts can start while their down matrices are
+// still on the way; returns the batch number in *batch (-1 when nothing was
+// loaded).
 cudaError_t load(moe_tier* t, const int32_t* ids, const int32_t* slot, const int32_t* kind, int n,
                  long long* batch) {
   *batch = -1;
@@ -137,20 +143,24 @@ cudaError_t load(moe_tier* t, const int32_t* ids, const int32_t* slot, const int
   cudaError_t e = cudaSuccess;
   // the slots being refilled may be read by the tier's last call
   if (t->any_call) e = cudaStreamWaitEvent(t->copy_s, t->call_done, 0);
-  for (int i = 0; i < n && e == cudaSuccess; ++i) {
-    if (kind[i] != moe::kSlotLoad) continue;
-    const size_t e_id = static_cast<size_t>(ids[i]), s = static_cast<size_t>(slot[i]);
-    for (int m = 0; m < kMats && e == cudaSuccess; ++m) {
-      e = cudaMemcpyAsync(t->slot_base[m] + s * t->mat_bytes[m],
-                          t->host_base[m] + e_id * t->mat_bytes[m], t->mat_bytes[m],
-                          cudaMemcpyHostToDevice, t->copy_s);
-      t->h2d += t->mat_bytes[m];
+  const long long b = t->n_batches;
+  // matrices 0-3: gate and up weights and scales; 4-5: down
+  for (int part = 0; part < 2 && e == cudaSuccess; ++part) {
+    for (int i = 0; i < n && e == cudaSuccess; ++i) {
+      if (kind[i] != moe::kSlotLoad) continue;
+      const size_t e_id = static_cast<size_t>(ids[i]), s = static_cast<size_t>(slot[i]);
+      for (int m = part * 4; m < (part ? kMats : 4) && e == cudaSuccess; ++m) {
+        e = cudaMemcpyAsync(t->slot_base[m] + s * t->mat_bytes[m],
+                            t->host_base[m] + e_id * t->mat_bytes[m], t->mat_bytes[m],
+                            cudaMemcpyHostToDevice, t->copy_s);
+        t->h2d += t->mat_bytes[m];
+      }
     }
+    if (e == cudaSuccess)
+      e = cudaEventRecord(part ? t->batch_ev[b % kRing] : t->gu_ev[b % kRing], t->copy_s);
   }
   if (e != cudaSuccess) return e;
-  const long long b = t->n_batches++;
-  e = cudaEventRecord(t->batch_ev[b % kRing], t->copy_s);
-  if (e != cudaSuccess) return e;
+  ++t->n_batches;
   for (int i = 0; i < n; ++i)
     if (kind[i] == moe::kSlotLoad) t->fill_batch[slot[i]] = b;
   *batch = b;
@@ -275,8 +285,10 @@ moe_status_t moe_tier_create(const moe_config_t* cfg, const moe_weights_t* w,
     return st;
   }
   e = cudaStreamCreateWithFlags(&t->copy_s, cudaStreamNonBlocking);
-  for (int i = 0; i < kRing && e == cudaSuccess; ++i)
+  for (int i = 0; i < kRing && e == cudaSuccess; ++i) {
     e = cudaEventCreateWithFlags(&t->batch_ev[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t->gu_ev[i], cudaEventDisableTiming);
+  }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t->call_done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMalloc(&t->d_tab, static_cast<size_t>(E) * 4);
   if (e == cudaSuccess) e = cudaMallocHost(&t->h_union, static_cast<size_t>(E + 1) * 4);
@@ -351,8 +363,11 @@ moe_status_t moe_tier_forward(moe_tier_t* t, const void* x, moe_dtype_t dtype, i
     if (e == cudaSuccess) e = moe::launch_down_slots(w, sh, T, ws, t->d_tab, 0, s);
   }
   if (e == cudaSuccess && wait >= 0) {
-    e = cudaStreamWaitEvent(s, t->batch_ev[wait % kRing], 0);
+    // batches land in order: the newest one the late experts need covers the
+    // older ones, its gate/up part before its down part
+    e = cudaStreamWaitEvent(s, t->gu_ev[wait % kRing], 0);
     if (e == cudaSuccess) e = moe::launch_gate_up_slots(w, sh, T, ws, t->d_tab, 1, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, t->batch_ev[wait % kRing], 0);
     if (e == cudaSuccess) e = moe::launch_down_slots(w, sh, T, ws, t->d_tab, 1, s);
   }
   if (e == cudaSuccess) e = moe::launch_combine(sh, T, ws, y, accumulate, s);
