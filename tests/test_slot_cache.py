@@ -178,3 +178,62 @@ def test_random_sequence_matches_the_model(m, E, S, P, k, T):
             assert st[key] == v, (step, key)
         assert list(slot_of) == ref.slot_table(), step
         assert [int(u) for u in uses] == ref.uses, step
+
+
+class _MruModel(TierModel):
+    """Planted slip: evicts the most recently used slot."""
+
+    def _victim(self, cands):
+        return max(cands, key=lambda c: self.stamp[c])
+
+
+class _NoClockOnHitModel(TierModel):
+    """Planted slip: a hit does not refresh the use clock (FIFO, not LRU)."""
+
+    def admit(self, ids):
+        keep = list(self.stamp)
+        out = self._place(list(ids), True, False)
+        if out is not None:
+            for (s, kind) in out:
+                if kind != LOAD:
+                    self.stamp[s] = keep[s]
+        return out
+
+
+class _NoHysteresisModel(TierModel):
+    """Planted slip: a pin is replaced by any hotter expert."""
+
+    @staticmethod
+    def _swap_ok(hot_uses, cold_uses):
+        return hot_uses > cold_uses
+
+
+def _diverges(m, model_cls, E=64, S=20, P=4, k=4, T=3, steps=400, seed=5):
+    rng = np.random.default_rng(seed)
+    call = min(E, k * T)
+    c = m.SlotCache(E, S, P, call)
+    ref = model_cls(E, S, P, call)
+    c.pin([1, 2])
+    ref.pin([1, 2])
+    for step in range(steps):
+        if step % 25 == 24:
+            if c.repin(2) != ref.repin(2):
+                return True
+            continue
+        ids = _zipf_union(rng, E, k, int(rng.integers(1, T + 1)))
+        s, kk = c.admit(ids)
+        want = ref.admit(ids)
+        if want is None or [(int(a), int(b)) for a, b in zip(s, kk)] != want:
+            return True
+        if list(c.query()[1]) != ref.slot_table():
+            return True
+    return False
+
+
+@pytest.mark.parametrize("slip", [_MruModel, _NoClockOnHitModel, _NoHysteresisModel])
+def test_the_comparison_catches_planted_slips(m, slip):
+    """The randomised comparison has the power to see a wrong rule: each
+    planted slip in the Python statement makes it disagree with the library,
+    while the unmutated statement agrees (test_random_sequence_matches_the_model)."""
+    assert not _diverges(m, TierModel)
+    assert _diverges(m, slip)

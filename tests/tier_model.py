@@ -69,7 +69,7 @@ class TierModel:
                 else:
                     cands = [s for s in range(self.S)
                              if not self.pinned[s] and s not in held]
-                    s = min(cands, key=lambda c: self.stamp[c])
+                    s = self._victim(cands)
                     self.stats["evictions"] += 1
                 self.expert[s] = e
                 self.clock += 1
@@ -85,6 +85,10 @@ class TierModel:
                 self.uses[e] += 1
             out.append((s, kind))
         return out
+
+    def _victim(self, cands):
+        """The least recently used of the evictable slots."""
+        return min(cands, key=lambda c: self.stamp[c])
 
     def admit(self, ids):
         return self._place(list(ids), True, False)
@@ -115,11 +119,16 @@ class TierModel:
             h, c = hot(), cold()
             if h is None or c is None:
                 break
-            if not self.uses[self.expert[h]] > 1.25 * self.uses[self.expert[c]] + 4:
+            if not self._swap_ok(self.uses[self.expert[h]], self.uses[self.expert[c]]):
                 break
             self.pinned[c], self.pinned[h] = False, True
             changes += 1
         return changes
+
+    @staticmethod
+    def _swap_ok(hot_uses, cold_uses):
+        """Item 6's hysteresis: the hot expert must be 25 % + 4 uses ahead."""
+        return hot_uses > 1.25 * cold_uses + 4
 
     def slot_table(self):
         """slot_of per expert as the library reports it: slot, -(slot + 2)
