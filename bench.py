@@ -255,7 +255,7 @@ def make_workload(name, experts=None, calls=None, tokens=None):
     return wl
 
 
-class GpuRun:
+class DeviceRun:
     """Resident layers, inputs and outputs of one workload on one device."""
 
     def __init__(self, wl, dev, layers=None):
@@ -542,7 +542,7 @@ def measure(args, wl, dev, world, steps, warmup, clocks, min_timed_s=0.0, layers
 
     import torch
 
-    run = GpuRun(wl, dev, layers)
+    run = DeviceRun(wl, dev, layers)
     sh = wl.shape
     warm_ms = []
     for _ in range(max(warmup, 3)):
