@@ -45,6 +45,42 @@ int main(void) {
   CHECK(moe_selftest_desync(NULL) == MOE_ERR_INVALID_ARG);
   CHECK(moe_trace_phase_name(0) != NULL && moe_trace_phase_name(-1) == NULL);
   moe_destroy(NULL);
+  {
+    /* the expert tier's residency policy is plain host code: 8 experts,
+       4 slots, one of them for the hot store, calls of up to 2 experts */
+    moe_slot_cache_t* c = NULL;
+    moe_slot_cache_stats_t st;
+    int32_t a[2] = {3, 5}, b[2] = {6, 7}, d[2] = {5, 1}, slot[2], kind[2], where[8];
+    uint64_t uses[8];
+    moe_tier_t* t = (moe_tier_t*)1;
+    moe_tier_config_t tc = {4, 0};
+    CHECK(moe_slot_cache_create(8, 4, 1, 2, &c) == MOE_OK && c != NULL);
+    CHECK(moe_slot_cache_admit(c, a, 2, slot, kind) == MOE_OK);
+    CHECK(slot[0] == 0 && slot[1] == 1 && kind[0] == 2 && kind[1] == 2);
+    CHECK(moe_slot_cache_admit(c, d, 2, slot, kind) == MOE_OK);
+    CHECK(slot[0] == 1 && kind[0] == 1 && slot[1] == 2 && kind[1] == 2);
+    CHECK(moe_slot_cache_admit(c, b, 2, slot, kind) == MOE_OK);
+    CHECK(slot[0] == 3 && slot[1] == 0); /* expert 3 (oldest use) was evicted */
+    CHECK(moe_slot_cache_query(c, &st, where, uses) == MOE_OK);
+    CHECK(st.misses == 5 && st.hits_lru == 1 && st.evictions == 1 && st.n_resident == 4);
+    CHECK(where[3] == -1 && where[7] == 0 && uses[5] == 2);
+    a[1] = 3;
+    a[0] = 3; /* repeated id: refused, nothing changed */
+    CHECK(moe_slot_cache_admit(c, a, 2, slot, kind) == MOE_ERR_INVALID_ARG);
+    CHECK(moe_slot_cache_repin(NULL, 1) == -1);
+    moe_slot_cache_destroy(c);
+    /* the tier's checks come before any CUDA call: NULL weights, and 4
+       slots where 512 tokens of top-8 need all 256 experts to fit */
+    CHECK(moe_tier_create(&glm, NULL, &tc, &t) == MOE_ERR_INVALID_ARG && t == NULL);
+    {
+      moe_weights_t w;
+      memset(&w, 0, sizeof(w));
+      t = (moe_tier_t*)1;
+      CHECK(moe_tier_create(&glm, &w, &tc, &t) == MOE_ERR_INVALID_ARG && t == NULL);
+      CHECK(strstr(moe_last_error(NULL), "n_slots") != NULL);
+    }
+    moe_tier_destroy(NULL);
+  }
   printf("%s\n", fails ? "failed" : "ok");
   return fails != 0;
 }
