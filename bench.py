@@ -684,7 +684,8 @@ def measure(args, wl, dev, world, steps, warmup, clocks, min_timed_s=0.0, layers
 TIER_SLOTS, TIER_PINNED = 64, 16
 
 
-def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S):
+def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S, n_slots=TIER_SLOTS,
+                 n_pinned=TIER_PINNED):
     """glm_decode through the expert tier (moe_tier_forward).
 
     The first warm-up step fills the slots and the use counts; the hot store
@@ -721,7 +722,7 @@ def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S):
     step()
     resident_s = min(step() for _ in range(2))
     tier.close()
-    tier = m.ExpertTier(L, max_tokens=1, n_slots=TIER_SLOTS, n_pinned=TIER_PINNED,
+    tier = m.ExpertTier(L, max_tokens=1, n_slots=n_slots, n_pinned=n_pinned,
                         drop_device_routed=True)
     del L
     torch.cuda.empty_cache()
@@ -762,8 +763,8 @@ def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S):
             "workload": "glm_decode_tier", "hidden": sh.hidden, "inter": sh.inter,
             "n_experts": sh.n_experts, "top_k": sh.top_k, "tokens_per_call": 1,
             "calls_per_step": wl.calls, "tokens_per_step": wl.calls,
-            "hbm_slots": TIER_SLOTS, "pinned_slots": TIER_PINNED,
-            "host_store_bytes": sh.n_experts * eb, "hbm_slot_bytes": TIER_SLOTS * eb,
+            "hbm_slots": n_slots, "pinned_slots": n_pinned,
+            "host_store_bytes": sh.n_experts * eb, "hbm_slot_bytes": n_slots * eb,
             "weights": "int4 offset-binary, group 32, fp16 scales",
             "timing": "wall clock per step (routing, union read-back, slot decisions and "
                       "host-to-HBM expert copies inside), device synchronised at the end "
@@ -811,6 +812,10 @@ def main():
                     help="override tokens per call (profiling only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-records", action="store_true")
+    ap.add_argument("--tier-slots", type=int, default=TIER_SLOTS,
+                    help="HBM expert slots of the glm_decode_tier record")
+    ap.add_argument("--tier-pinned", type=int, default=TIER_PINNED,
+                    help="of which pinned (the hot store)")
     args = ap.parse_args()
     single = args.workload is not None
     name = args.workload or "glm_decode"
@@ -900,7 +905,8 @@ def run_tier_only(args):
     __graft_entry__.build()
     clocks = ClockSampler(0)
     clocks.start()
-    rec = measure_tier(dev, clocks, args.warmup)
+    rec = measure_tier(dev, clocks, args.warmup, n_slots=args.tier_slots,
+                       n_pinned=args.tier_pinned)
     clocks.stop()
     line = {"metric": METRIC, "n_gpus": 1, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
