@@ -211,3 +211,26 @@ def test_tier_create_validates_before_any_cuda_call(m):
     assert lib.moe_tier_forward(None, None, 0, 1, None, None, 0.0, 0, None, None) == -1
     assert lib.moe_tier_repin(None, 1, None) == -1
     lib.moe_tier_destroy(None)
+
+
+@pytest.mark.parametrize("E,k,T", [(16, 4, 1), (16, 4, 8), (256, 8, 1), (256, 8, 4), (64, 6, 3)])
+def test_tier_slot_rule(m, E, k, T):
+    """n_slots - n_pinned must hold one call's union, min(E, max_tokens * k):
+    one slot fewer is refused for its slot count; exactly enough passes that
+    check and stops at the next one (the fake routed pointers are not
+    page-locked host memory)."""
+    lib = m.load()
+    need = min(E, T * k)
+    cfg = _cfg(m, n_experts=E, top_k=k, n_group=1, topk_group=1, max_tokens=T)
+    h = C.c_void_p()
+    for pinned in (0, 2):
+        if need + pinned > E:
+            continue
+        tc = m.moe.moe_tier_config_t(need + pinned - 1, pinned)
+        assert lib.moe_tier_create(C.byref(cfg), C.byref(_fake_weights(m)), C.byref(tc),
+                                   C.byref(h)) == -1
+        assert b"n_slots" in lib.moe_last_error(None)
+        tc = m.moe.moe_tier_config_t(need + pinned, pinned)
+        assert lib.moe_tier_create(C.byref(cfg), C.byref(_fake_weights(m)), C.byref(tc),
+                                   C.byref(h)) == -1
+        assert b"page-locked" in lib.moe_last_error(None) and not h.value
