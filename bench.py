@@ -722,6 +722,7 @@ def measure_tier(dev, clocks, warmup, min_timed_s=SUB_MIN_TIMED_S, n_slots=TIER_
     step()
     resident_s = min(step() for _ in range(2))
     tier.close()
+    tier = None  # its pinned host copy is released before the next one is made
     tier = m.ExpertTier(L, max_tokens=1, n_slots=n_slots, n_pinned=n_pinned,
                         drop_device_routed=True)
     del L
